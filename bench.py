@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark: absorbed MLA decode on B300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+A step is one decode step of the hot path over one synthetic batch: the
+paged absorbed attention kernel and, when the batch is cut across SMs, its
+log-sum-exp combine kernel (both launched by one mla_decode_attn call).  The
+default workload is 64 sequences x 128 heads x 4096 cached positions
+(d_c = 512, d_r = 64, bf16, pages of 64 rows at a random permutation of the
+pool).  Inputs are generated on the device before timing; the 302 MB cache is
+larger than the 126 MB L2, so no flush is inserted between steps.
+
+value   : whole-job TFLOP/s = 2*(d_c+d_r) + 2*d_c FLOPs per (query, head,
+          visible cached row), summed over all ranks, / max-over-ranks time.
+e2e     : the same metric through the same call with the step's inputs
+          (q_lat, q_pe, seq_lens, page_table) copied from pinned host memory
+          and the result (o, lse) copied back, inside the timed region.
+roofline: the attention kernel alone, timed with CUDA events recorded around
+          it by the library (mla_set_decode_events), against the measured HBM
+          bandwidth (cache bytes) or bf16 tensor peak, whichever bound is
+          slower for this workload.
+
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+(the decode path has no exchange step): weak scaling, no collective on the
+data path.  --impl reference times the fp64 CPU oracle on the host cores on
+a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_latent_kv_71_b300 import workloads  # noqa: E402
+
+METRIC = ("MLA absorbed decode TFLOP/s + cache GB/s, % of B300 roofline "
+          "(B=64,H=128,L=4096)")
+DEFAULT_WORKLOAD = "decode_b64_h128_l4096"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ------------------------------------------------------------------ helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work_of(case: workloads.DecodeCase):
+    """(FLOPs, cache bytes) of one decode step: per visible (query, head, row)
+    2*(d_c+d_r) + 2*d_c FLOPs; every cached row (d_c + d_r bf16) read once."""
+    B, T, H, d_c = case.q_lat.shape
+    d_r = case.q_pe.shape[3]
+    lens = case.seq_lens.cpu().tolist()
+    rows = 0
+    for n in lens:
+        for t in range(T):
+            rows += max(0, n - (T - 1 - t)) if case.causal else n
+    flops = rows * H * (2 * (d_c + d_r) + 2 * d_c)
+    cache_bytes = sum(lens) * (d_c + d_r) * case.pool.element_size()
+    return flops, cache_bytes
+
+
+class ClockSampler:
+    """Polls NVML (SM clock, max clock, throttle reasons) in a thread."""
+
+    REASONS = {
+        "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+        "hw_power_brake_slowdown": 0x80, "sw_power_cap": 0x4,
+    }
+
+    def __init__(self, device_index: int):
+        self.samples, self.reasons, self.ok = [], set(), False
+        self.max_mhz = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(device_index).uuid)
+            try:
+                self.h = pynvml.nvmlDeviceGetHandleByUUID(uuid)
+            except Exception:
+                self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.nv = pynvml
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception as e:  # pragma: no cover - no NVML
+            self.err = repr(e)
+        self._stop = threading.Event()
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
+                mask = self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.ok:
+            self.t = threading.Thread(target=self._run, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self.ok:
+            self.t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "note": "no NVML samples"}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def traffic_record(kernel_src_sha: str):
+    """DRAM bytes per launch of the attention kernel from a committed ncu
+    capture, or None if absent or taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None, None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_src_sha256") != kernel_src_sha:
+        return None, "stale"
+    return d.get("dram_bytes_per_launch"), d.get("source")
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("decode_bf16.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mla_latent_kv_71_b300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def compact_sample(case: workloads.DecodeCase, nb: int):
+    """First nb sequences of a case with their pages gathered into a small
+    CPU pool (for timing the CPU oracle without copying the whole cache)."""
+    table = case.page_table[:nb]
+    used = table[table >= 0].long()
+    pool = case.pool[used.to(case.pool.device)].cpu()
+    new_table = torch.full_like(table.cpu(), -1)
+    new_table[(table >= 0).cpu()] = torch.arange(used.numel(), dtype=torch.int32)
+    return workloads.DecodeCase(case.q_lat[:nb].cpu(), case.q_pe[:nb].cpu(), pool, new_table,
+                                case.seq_lens[:nb].cpu(), case.scale, case.causal)
+
+
+def time_oracle(sample: workloads.DecodeCase):
+    import oracle
+    lib = oracle.load()
+    t0 = time.perf_counter()
+    oracle.decode_attn(sample.q_lat, sample.q_pe, sample.pool, sample.page_table,
+                       sample.seq_lens, sample.scale, causal=sample.causal, lib=lib)
+    return time.perf_counter() - t0
+
+
+def oracle_threads() -> int:
+    n = os.environ.get("OMP_NUM_THREADS")
+    return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
+
+
+def cpu_baseline(case: workloads.DecodeCase, budget_s: float = 15.0):
+    """The oracle as it stands on the host cores, on the first sequences of
+    the workload (calibrated to about budget_s of CPU work)."""
+    B = case.q_lat.shape[0]
+    one = compact_sample(case, 1)
+    t1 = time_oracle(one)
+    nb = max(1, min(B, int(budget_s / max(t1, 1e-3))))
+    sample = compact_sample(case, nb) if nb > 1 else one
+    t = time_oracle(sample) if nb > 1 else t1
+    flops, _ = work_of(sample)
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(),
+            "kind": "oracle",
+            "sample": f"first {nb} of {B} sequences (all heads, all positions), fp64, "
+                      f"{t:.2f} s"}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local):
+    from mla_latent_kv_71_b300 import mla
+    dev = torch.device("cuda", local)
+    case = workloads.make_workload(args.workload, device=dev)
+    B, T, H, d_c = case.q_lat.shape
+    flops, cache_bytes = work_of(case)
+    o = torch.empty_like(case.q_lat)
+    lse = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, mla.decode_workspace_size(B, T, H, d_c, case.q_lat.dtype)),
+                     dtype=torch.uint8, device=dev)
+    lens_host = case.seq_lens.cpu()
+
+    def step():
+        mla.decode_attn(case.q_lat, case.q_pe, case.pool, case.page_table, case.seq_lens,
+                        case.scale, causal=case.causal, o=o, lse=lse, workspace=ws,
+                        seq_lens_host=lens_host)
+
+    # kernels per step: attention + combine when the plan cuts a sequence
+    s = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = mla.launch_count()
+    with clocks, torch.cuda.stream(s):
+        t_start.record(s)
+        for i in range(args.steps):
+            mla.set_decode_events(*ev_attn[i])
+            step()
+        t_end.record(s)
+        torch.cuda.synchronize(dev)
+    mla.set_decode_events(None, None)
+    launches = mla.launch_count() - launches0
+    barrier(world)
+    step_ms = t_start.elapsed_time(t_end) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
+    code, detail = mla.get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail:#x}")
+
+    # ---- end to end through the same call, host buffers, copies inside
+    h_q = case.q_lat.cpu().pin_memory()
+    h_pe = case.q_pe.cpu().pin_memory()
+    h_lens = case.seq_lens.cpu().pin_memory()
+    h_table = case.page_table.cpu().pin_memory()
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    d_q, d_pe = torch.empty_like(case.q_lat), torch.empty_like(case.q_pe)
+    d_lens, d_table = torch.empty_like(case.seq_lens), torch.empty_like(case.page_table)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_pe, h_lens, h_table))
+    d2h = h_o.numel() * h_o.element_size() + h_lse.numel() * h_lse.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_pe.copy_(h_pe, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        d_table.copy_(h_table, non_blocking=True)
+        mla.decode_attn(d_q, d_pe, case.pool, d_table, d_lens, case.scale, causal=case.causal,
+                        o=o, lse=lse, workspace=ws, seq_lens_host=h_lens)
+        h_o.copy_(o, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    e_steps = max(3, min(args.steps, 200))
+    with torch.cuda.stream(s):
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for _ in range(e_steps):
+            e2e_step()
+        e1.record(s)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e_steps, world)
+
+    pk, pk_kind = peaks()
+    t_flop = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = cache_bytes / (pk["hbm_gbs"] * 1e9)
+    attn_s = attn_ms * 1e-3
+    traffic, _ = traffic_record(kernel_sha())
+    if t_hbm >= t_flop:
+        roof = {"bound": "hbm", "achieved": cache_bytes / attn_s / 1e9, "peak": pk["hbm_gbs"],
+                "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / attn_s / 1e12, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = traffic
+    roof["kernel"] = "decode_bf16_kernel"
+    roof["peak_kind"] = f"{pk_kind} (burst)"
+    roof["algorithmic_bytes_per_launch"] = cache_bytes
+    roof["algorithmic_flops_per_launch"] = flops
+    roof["attn_us"] = attn_ms * 1e3
+    roof["roofline_us"] = max(t_flop, t_hbm) * 1e6
+    roof["pct_roofline_attn"] = max(t_flop, t_hbm) / attn_s
+    roof["pct_roofline_step"] = max(t_flop, t_hbm) / (step_ms * 1e-3)
+    roof["tensor_frac_attn"] = flops / attn_s / 1e12 / pk["bf16_tflops"]
+
+    value = flops * world / (step_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "T": T, "H": H, "d_c": d_c,
+                   "d_r": case.q_pe.shape[3], "page": case.pool.shape[1],
+                   "cached_positions": int(case.seq_lens.sum()),
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (cache %.0f MB > 126 MB); no flush" %
+                         (cache_bytes / 1e6)},
+        "cache_gbs": cache_bytes * world / (step_ms * 1e-3) / 1e9,
+        "pct_roofline": max(t_flop, t_hbm) / (step_ms * 1e-3),
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches,
+        "roofline": roof,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case)
+    return line
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args, rank, world):
+    """The fp64 oracle on the host cores, on a bounded sample per step."""
+    spec = workloads.WORKLOADS[args.workload]
+    full = workloads.make_workload(args.workload, device="cpu", B=1)
+    t1 = time_oracle(full)
+    B = spec["B"]
+    nb = max(1, min(B, int(args.ref_step_s / max(t1, 1e-3))))
+    sample = workloads.make_workload(args.workload, device="cpu", B=nb)
+    flops, _ = work_of(sample)
+    for _ in range(args.warmup if args.warmup < 2 else 1):
+        time_oracle(sample)
+    times = [time_oracle(sample) for _ in range(args.steps)]
+    t = statistics.mean(times)
+    value = flops / t / 1e12
+    lens = workloads.workload_lens(spec)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "T": spec["T"], "H": spec["H"],
+                   "d_c": spec["d_c"], "d_r": spec["d_r"], "page": workloads.PAGE,
+                   "cached_positions": int(sum(lens)), "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle_threads(),
+                         "kind": "oracle",
+                         "sample": f"each step: first {nb} of {B} sequences, all heads, fp64"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-step-s", type=float, default=5.0,
+                    help="reference arm: CPU seconds per step (sample size)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,204 @@
+/*
+ * mla.h -- C ABI of libmla: weight-absorbed Multi-head Latent Attention (MLA)
+ * decode for NVIDIA B300 (sm_103a).
+ *
+ * The decode step of one attention layer, for query token t of sequence b and
+ * head i, against the cached rows [c_j ; k^R_j] of positions j:
+ *
+ *   q_lat_i = W^UK_i^T q^C_i                                   mla_absorb_q
+ *   s_ij    = (q_lat_i . c_j + q^R_i . k^R_j) * scale          mla_decode_attn
+ *   o_i     = sum_j softmax_j(s_ij) c_j,  lse_i = ln sum_j e^{s_ij}
+ *   (pieces of one softmax merged by log-sum-exp)              mla_combine_splits
+ *   out     = W^O concat_i (W^UV_i o_i)                        mla_out_proj
+ *
+ * Sources (web pages on MLA):
+ *   [Mishra] "Multi-head Latent Attention", Neel Mishra: sections "Step 2:
+ *            absorb the up-projections" and "Step 4: decoupled RoPE".
+ *   [Zhang]  zhangchitc.github.io MLA post: "Matrix absorption: compression
+ *            that also saves compute", "Decoupled RoPE", "Value absorption:
+ *            weight and sum first, project after".
+ *   [llms]   "Multi-Head Latent Attention: How Low-Rank KV Compression
+ *            Scales LLM Serving": "Low-Rank Key-Value Joint Compression",
+ *            "Query Key Absorption", "Value Output Absorption".
+ *
+ * Conventions for every entry point:
+ *   - Pointers are device pointers unless the name ends in _host.  All
+ *     buffers, workspaces included, are owned by the caller; the library
+ *     allocates no device memory.  Tensors are dense, row-major, in the
+ *     stated shape, and 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *   - Argument errors are returned before anything is launched.  Errors found
+ *     on the device (a bounded wait that gave up, an out-of-range page id or
+ *     length) raise a device status word that mla_get_device_status() reads;
+ *     while it is raised, later calls' kernels return without results.
+ *   - dtype MLA_BF16: bf16 tensors (except lse and partials, always fp32),
+ *     tensor-core (tcgen05) kernels, fp32 accumulation.  dtype MLA_FP32: fp32
+ *     tensors, CUDA-core kernels in fp32.  Shapes the bf16 kernels do not
+ *     cover return MLA_ERR_UNSUPPORTED; there is no fallback.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream). */
+typedef struct CUstream_st* mla_stream_t;
+
+typedef enum mla_status {
+    MLA_OK = 0,
+    MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment, short workspace */
+    MLA_ERR_UNSUPPORTED = 2,   /* valid shape the kernels of this dtype do not cover    */
+    MLA_ERR_CUDA = 3,          /* a CUDA runtime call failed (launch or query)          */
+    MLA_ERR_TIMEOUT = 4,       /* device: a bounded wait gave up                         */
+    MLA_ERR_DEVICE_BOUNDS = 5  /* device: page id or sequence length out of range       */
+} mla_status_t;
+
+typedef enum mla_dtype { MLA_BF16 = 0, MLA_FP32 = 1 } mla_dtype_t;
+
+/*
+ * mla_absorb_q -- query-side weight absorption, per head:
+ *     q_lat[r, i, :] = W^UK_i^T q_nope[r, i, :]
+ * ([llms] "Query Key Absorption"; [Mishra] "Step 2: absorb the
+ * up-projections"; [Zhang] "Matrix absorption": the up-projection is applied
+ * once to the query instead of to every cached latent.)
+ *
+ *   q_nope [rows, H, d_h]   content part of the query (q^C), rows = B*T
+ *   w_uk   [H, d_h, d_c]    W^UK in R^{H*d_h x d_c}; head i owns rows
+ *                            i*d_h .. (i+1)*d_h-1
+ *   q_lat  [rows, H, d_c]   output
+ * bf16: d_c % 128 == 0, d_h % 64 == 0, rows >= 1.
+ */
+mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int rows, int H,
+                          int d_h, int d_c, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * Bytes of device workspace mla_decode_attn needs for this shape on the
+ * current device (0 for MLA_FP32).  The content need not be initialised.
+ */
+size_t mla_decode_workspace_size(int B, int T, int H, int d_c, mla_dtype_t dtype);
+
+/*
+ * mla_decode_attn -- absorbed decode attention against a paged latent cache.
+ * For every sequence b, query token t < T and head i < H:
+ *     s_j  = (q_lat[b,t,i,:] . c_j + q_pe[b,t,i,:] . k^R_j) * scale
+ *     o    = sum_j softmax_j(s) c_j,     lse = ln sum_j exp(s_j)
+ * over the visible positions j: 0 .. seq_lens[b]-1, or with causal != 0,
+ * 0 .. seq_lens[b]-T+t (query t sits at position seq_lens[b]-T+t).
+ * ([llms] "Query Key Absorption": scores of the absorbed query against the
+ * cached latent plus the decoupled RoPE term; [Zhang] "Decoupled RoPE" and
+ * "Value absorption": the sum is scaled (the pages use 1/sqrt(d_h + d_r))
+ * and soft-maxed, and the weights mix the latents c_j, which are never
+ * expanded to keys or values; [Mishra] "Step 4: decoupled RoPE": the cache
+ * row is [c_j ; k^R_j], d_c + d_r numbers shared by all heads.)
+ * A query that sees no position gets o = 0 and lse = -inf.
+ *
+ *   q_lat      [B, T, H, d_c]            absorbed content query
+ *   q_pe       [B, T, H, d_r]            RoPE query (already rotated)
+ *   kv_pool    [num_pages, page_size, d_c + d_r]   cache rows [c ; k^R]
+ *                                        (k^R already rotated); rows past a
+ *                                        sequence's length are ignored and
+ *                                        may hold anything
+ *   page_table [B, max_pages] int32      position j of sequence b is row
+ *                                        j % page_size of pool page
+ *                                        page_table[b][j / page_size];
+ *                                        entries past the last page unused
+ *   seq_lens   [B] int32 (device)        cached positions per sequence
+ *   seq_lens_host [B] int32 or NULL      the same lengths in host memory; when
+ *                                        given, the combine launch is skipped
+ *                                        if no sequence is split
+ *   o          [B, T, H, d_c]            output (dtype)
+ *   lse        [B, T, H] fp32            output, natural log
+ *   workspace  >= mla_decode_workspace_size(B, T, H, d_c, dtype) bytes
+ * bf16 kernels: d_c == 512, d_r == 64, page_size == 64, any H >= 1 (heads
+ * are processed in groups of 128), any T >= 1.  The fp32 kernels take
+ * d_c <= 512 (multiple of 4), d_r <= 64, any page_size.
+ * Work is balanced over all SMs: long or ragged sequences are split across
+ * SMs and merged by log-sum-exp inside this call (a second kernel).
+ */
+mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv_pool,
+                             const int32_t* page_table, const int32_t* seq_lens,
+                             const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                             int d_r, int page_size, int max_pages, int64_t num_pages,
+                             float scale, int causal, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * mla_combine_splits -- merge S partial results of the same softmax rows,
+ * each computed over a disjoint subset of the cached positions:
+ *     lse = ln sum_s exp(lse_part[s]),   o = sum_s exp(lse_part[s] - lse) o_part[s]
+ * A piece with lse_part = -inf carries weight 0; rows whose pieces are all
+ * empty get o = 0, lse = -inf.  (The pages define one softmax over all
+ * cached positions; this is the same softmax assembled from pieces.)
+ *
+ *   o_part   [S, rows, d_c] fp32   normalised partial outputs
+ *   lse_part [S, rows] fp32        their log-sum-exps
+ *   o        [rows, d_c] (dtype),  lse [rows] fp32
+ * d_c % 4 == 0, 1 <= S <= 1024.
+ */
+mla_status_t mla_combine_splits(const float* o_part, const float* lse_part, int S, int64_t rows,
+                                int d_c, void* o, float* lse, mla_dtype_t dtype,
+                                mla_stream_t stream);
+
+/*
+ * Bytes of device workspace mla_out_proj needs (0 for MLA_FP32).  The
+ * workspace must be zero-filled before its first use; every call leaves its
+ * counters at zero again.
+ */
+size_t mla_out_proj_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t dtype);
+
+/*
+ * mla_out_proj -- output side of the absorbed layer:
+ *     v[r, i*d_h : (i+1)*d_h] = W^UV_i o[r, i, :]          (d_c -> d_h per head)
+ *     out[r, :]                = W^O v[r, :]               (H*d_h -> d)
+ * ([llms] "Value Output Absorption"; [Zhang] "Value absorption": W^UV is
+ * pulled out of the weighted sum and applied once; the two weights are kept
+ * apart rather than merged into one larger matrix.)
+ *
+ *   o     [rows, H, d_c]     latent outputs of mla_decode_attn
+ *   w_uv  [H, d_h, d_c]      W^UV, head i owns rows i*d_h .. (i+1)*d_h-1
+ *   w_o   [d, H*d_h]         W^O
+ *   v_tmp [rows, H*d_h]      intermediate (dtype), caller-owned
+ *   out   [rows, d]          output (dtype)
+ * bf16: d_h % 128 == 0, d_c % 64 == 0, d % 128 == 0.
+ */
+mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void* v_tmp,
+                          void* out, int rows, int H, int d_h, int d_c, int d, void* workspace,
+                          size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the current device's status
+ * word.  Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (or
+ * MLA_ERR_CUDA if the synchronisation itself failed).  If detail is not NULL
+ * it receives the word's detail field (where the error was found).
+ */
+mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail);
+
+/*
+ * Timing hook: while set (both non-NULL), every bf16 mla_decode_attn call
+ * records `start` on its stream just before its attention kernel and `end`
+ * just after it, so that a caller can time that kernel apart from the
+ * combine kernel of the same call.  Arguments are CUDA events (cudaEvent_t)
+ * owned by the caller; NULL, NULL clears the hook.  Process-wide, not
+ * thread-safe against concurrent decode calls.
+ */
+void mla_set_decode_events(void* start, void* end);
+
+/* Number of kernels this library has launched in this process so far. */
+uint64_t mla_launch_count(void);
+
+/* Static description of a status code. */
+const char* mla_status_string(mla_status_t status);
+
+/* Library ABI version (major * 100 + minor). */
+int mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,491 @@
+// mla_lib.cu -- the C ABI of libmla (declared in include/mla.h): argument
+// checks, TMA tensor maps, work planning and kernel launches.  The library is
+// one translation unit so that the device status word has a single home.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mla.h"
+#include "decode_bf16.cuh"
+#include "gemm_bf16.cuh"
+#include "kernels_fp32.cuh"
+#include "ptx.cuh"
+#include "status.cuh"
+
+namespace {
+
+using mla::dec::Params;
+
+constexpr int kMaxDevices = 64;
+
+// Caller-owned events recorded around the decode attention kernel (see
+// mla_set_decode_events); both null when unset.
+cudaEvent_t g_ev_start = nullptr, g_ev_end = nullptr;
+
+// Kernels launched by this library (reported by mla_launch_count).
+std::atomic<uint64_t> g_launches{0};
+
+// ------------------------------------------------------------ driver entry
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Tiled bf16 tensor map; dims/strides innermost first, strides in bytes.
+bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint32_t es[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box,
+              es, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------ device facts
+
+struct DeviceInfo {
+    bool ready = false;
+    int sms = 0;
+    int decode_clusters = 0;  // co-resident 2-CTA clusters of the decode kernel
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool device_info(DeviceInfo& out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return false;
+        if (cudaFuncSetAttribute(mla::dec::decode_bf16_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mla::dec::SMEM_ALLOC) != cudaSuccess)
+            return false;
+        if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 200 * 1024) != cudaSuccess)
+            return false;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
+        cfg.blockDim = dim3(mla::dec::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = mla::dec::SMEM_ALLOC;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, mla::dec::decode_bf16_kernel, &cfg) != cudaSuccess ||
+            n <= 0) {
+            cudaGetLastError();
+            n = d.sms / 2;
+        }
+        d.decode_clusters = n;
+        d.ready = true;
+    }
+    out = d;
+    return true;
+}
+
+// ------------------------------------------------------------------ checks
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Status of the launch(es) just made; counts `n` launched kernels.
+mla_status_t launch_status(int n = 1) {
+    if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+    g_launches += n;
+    return MLA_OK;
+}
+
+// ------------------------------------------------------------ decode plan
+
+// Host copy of the kernel's range arithmetic: does any unit straddle two
+// clusters (or see no position)?  Used only to skip the combine launch.
+bool host_plan_needs_combine(const int32_t* lens, int B, int T, int HG, int max_pages, int causal,
+                             int64_t G) {
+    std::vector<int64_t> pages;
+    pages.reserve((size_t)B * T * HG);
+    int64_t total = 0;
+    for (int b = 0; b < B; ++b) {
+        int64_t len = lens[b];
+        if (len < 0 || len > (int64_t)max_pages * 64) return true;
+        for (int t = 0; t < T; ++t) {
+            int64_t n = causal ? len - (T - 1 - t) : len;
+            if (n <= 0) return true;
+            for (int hg = 0; hg < HG; ++hg) {
+                pages.push_back((n + 63) / 64);
+                total += (n + 63) / 64;
+            }
+        }
+    }
+    auto cl = [&](int64_t x) {
+        int64_t g = x * G / total;
+        while (g + 1 < G && total * (g + 1) / G <= x) ++g;
+        while (g > 0 && total * g / G > x) --g;
+        return g;
+    };
+    int64_t pos = 0;
+    for (int64_t n : pages) {
+        if (cl(pos) != cl(pos + n - 1)) return true;
+        pos += n;
+    }
+    return false;
+}
+
+struct DecodeWs {
+    size_t unit_off, lse_off, o_off, total;
+};
+
+DecodeWs decode_ws_layout(int64_t U, int64_t G, int d_c) {
+    auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const int64_t slots = G + U;
+    DecodeWs w;
+    w.unit_off = 0;
+    w.lse_off = up(sizeof(int2) * (size_t)U);
+    w.o_off = up(w.lse_off + sizeof(float) * (size_t)slots * mla::dec::HEADS);
+    w.total = up(w.o_off + sizeof(float) * (size_t)slots * mla::dec::HEADS * (size_t)d_c);
+    return w;
+}
+
+// ------------------------------------------------------------- GEMM plan
+
+struct GemmPlan {
+    int BN, n_tiles, splits, chunks;
+    size_t ws_part_bytes, ws_count_bytes;
+};
+
+GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, bool allow_split) {
+    GemmPlan g;
+    g.BN = N >= 256 ? 256 : ((N + 15) / 16) * 16;
+    g.n_tiles = (N + g.BN - 1) / g.BN;
+    const int chunks_total = K / mla::gemm::BK;
+    const int tiles = (M / mla::gemm::BM) * Z * g.n_tiles;
+    int splits = 1;
+    if (allow_split) {
+        const int target = 2 * sms;  // two CTAs fit per SM
+        splits = (target + tiles / 2) / tiles;
+        if (splits < 1) splits = 1;
+        if (splits > chunks_total) splits = chunks_total;
+    }
+    g.chunks = (chunks_total + splits - 1) / splits;
+    g.splits = (chunks_total + g.chunks - 1) / g.chunks;
+    g.ws_part_bytes = g.splits > 1 ? sizeof(float) * (size_t)g.splits * Z * N * M : 0;
+    g.ws_count_bytes = g.splits > 1 ? sizeof(int) * (size_t)tiles : 0;
+    return g;
+}
+
+mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tx, int M, int N, int K, int Z,
+                         int a_mn, int x_batched, const GemmPlan& g, __nv_bfloat16* out,
+                         int64_t ldo, int64_t out_z, float* ws_part, int* ws_count,
+                         cudaStream_t st) {
+    mla::gemm::Params p;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.BN = g.BN;
+    p.n_tiles = g.n_tiles;
+    p.a_mn = a_mn;
+    p.x_batched = x_batched;
+    p.splits = g.splits;
+    p.chunks_per_split = g.chunks;
+    p.out = out;
+    p.ldo = ldo;
+    p.out_z = out_z;
+    p.ws_part = ws_part;
+    p.ws_count = ws_count;
+    const size_t smem = (size_t)mla::gemm::STAGES * (mla::gemm::A_BYTES + g.BN * mla::gemm::BK * 2) +
+                        256 + 1024;
+    dim3 grid(M / mla::gemm::BM, Z * g.n_tiles, g.splits);
+    mla::gemm::wgemm_kernel<<<grid, mla::gemm::THREADS, smem, st>>>(ta, tx, p);
+    return launch_status();
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+int mla_version(void) { return 100; }
+
+uint64_t mla_launch_count(void) { return g_launches.load(); }
+
+void mla_set_decode_events(void* start, void* end) {
+    g_ev_start = static_cast<cudaEvent_t>(start);
+    g_ev_end = static_cast<cudaEvent_t>(end);
+}
+
+const char* mla_status_string(mla_status_t s) {
+    switch (s) {
+        case MLA_OK: return "ok";
+        case MLA_ERR_INVALID_ARG: return "invalid argument";
+        case MLA_ERR_UNSUPPORTED: return "unsupported shape for this dtype";
+        case MLA_ERR_CUDA: return "CUDA runtime error";
+        case MLA_ERR_TIMEOUT: return "device: bounded wait timed out";
+        case MLA_ERR_DEVICE_BOUNDS: return "device: page id or sequence length out of range";
+    }
+    return "unknown status";
+}
+
+mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail) {
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    uint32_t w = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&w, mla::g_device_status, sizeof w) != cudaSuccess) return MLA_ERR_CUDA;
+    if (w != 0 && cudaMemcpyToSymbol(mla::g_device_status, &zero, sizeof zero) != cudaSuccess)
+        return MLA_ERR_CUDA;
+    if (detail) *detail = w >> 8;
+    switch (w & 0xFFu) {
+        case mla::MLA_DEV_OK: return MLA_OK;
+        case mla::MLA_DEV_TIMEOUT: return MLA_ERR_TIMEOUT;
+        default: return MLA_ERR_DEVICE_BOUNDS;
+    }
+}
+
+// ------------------------------------------------------------ mla_absorb_q
+
+mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int rows, int H,
+                          int d_h, int d_c, mla_dtype_t dtype, mla_stream_t stream) {
+    if (!q_nope || !w_uk || !q_lat || rows < 1 || H < 1 || d_h < 1 || d_c < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == MLA_FP32) {
+        dim3 grid((unsigned)rows * H, (d_c + 127) / 128);
+        mla::absorb_q_fp32_kernel<<<grid, 128, 0, st>>>(
+            static_cast<const float*>(q_nope), static_cast<const float*>(w_uk),
+            static_cast<float*>(q_lat), rows, H, d_h, d_c);
+        return launch_status();
+    }
+    if (dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (d_c % 128 != 0 || d_h % 64 != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const GemmPlan g = gemm_plan(d_c, rows, d_h, H, di.sms, false);
+    // A = W^UK_i^T, stored along d_c: MN-major tiles [64 d_h rows x 64 d_c]
+    CUtensorMap ta, tx;
+    cuuint64_t ad[3] = {(cuuint64_t)d_c, (cuuint64_t)d_h, (cuuint64_t)H};
+    cuuint64_t as[2] = {(cuuint64_t)d_c * 2, (cuuint64_t)d_h * d_c * 2};
+    cuuint32_t ab[3] = {64, 64, 1};
+    cuuint64_t xd[3] = {(cuuint64_t)d_h, (cuuint64_t)H, (cuuint64_t)rows};
+    cuuint64_t xs[2] = {(cuuint64_t)d_h * 2, (cuuint64_t)H * d_h * 2};
+    cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g.BN};
+    if (!make_map(&ta, w_uk, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tx, q_nope, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLA_ERR_CUDA;
+    return launch_gemm(ta, tx, d_c, rows, d_h, H, 1, 1, g, static_cast<__nv_bfloat16*>(q_lat),
+                       (int64_t)H * d_c, d_c, nullptr, nullptr, st);
+}
+
+// ------------------------------------------------------------ mla_out_proj
+
+size_t mla_out_proj_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || rows < 1 || H < 1 || d_h < 1 || d < 128) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    const GemmPlan g = gemm_plan(d, rows, H * d_h, 1, di.sms, true);
+    return ((g.ws_part_bytes + 255) & ~size_t(255)) + g.ws_count_bytes;
+}
+
+mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void* v_tmp, void* out,
+                          int rows, int H, int d_h, int d_c, int d, void* workspace,
+                          size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream) {
+    if (!o || !w_uv || !w_o || !v_tmp || !out || rows < 1 || H < 1 || d_h < 1 || d_c < 1 || d < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(w_uv) || !aligned16(w_o) || !aligned16(v_tmp) ||
+        !aligned16(out))
+        return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == MLA_FP32) {
+        const int64_t warps1 = (int64_t)rows * H * d_h, warps2 = (int64_t)rows * d;
+        mla::out_proj_v_fp32_kernel<<<(unsigned)((warps1 + 3) / 4), 128, 0, st>>>(
+            static_cast<const float*>(o), static_cast<const float*>(w_uv), static_cast<float*>(v_tmp),
+            rows, H, d_h, d_c);
+        mla::out_proj_o_fp32_kernel<<<(unsigned)((warps2 + 3) / 4), 128, 0, st>>>(
+            static_cast<const float*>(v_tmp), static_cast<const float*>(w_o), static_cast<float*>(out),
+            rows, H * d_h, d);
+        return launch_status(2);
+    }
+    if (dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (d_h % 128 != 0 || d_c % 64 != 0 || d % 128 != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const int K2 = H * d_h;
+    const GemmPlan g1 = gemm_plan(d_h, rows, d_c, H, di.sms, false);
+    const GemmPlan g2 = gemm_plan(d, rows, K2, 1, di.sms, true);
+    const size_t part_bytes = (g2.ws_part_bytes + 255) & ~size_t(255);
+    if (g2.splits > 1 && (!workspace || workspace_bytes < part_bytes + g2.ws_count_bytes ||
+                          !aligned16(workspace)))
+        return MLA_ERR_INVALID_ARG;
+    CUtensorMap ta1, tx1, ta2, tx2;
+    {   // v = W^UV_i o_i : A K-major [d_h rows x 64 d_c], X = o [rows, H, d_c]
+        cuuint64_t ad[3] = {(cuuint64_t)d_c, (cuuint64_t)d_h, (cuuint64_t)H};
+        cuuint64_t as[2] = {(cuuint64_t)d_c * 2, (cuuint64_t)d_h * d_c * 2};
+        cuuint32_t ab[3] = {64, 128, 1};
+        cuuint64_t xd[3] = {(cuuint64_t)d_c, (cuuint64_t)H, (cuuint64_t)rows};
+        cuuint64_t xs[2] = {(cuuint64_t)d_c * 2, (cuuint64_t)H * d_c * 2};
+        cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g1.BN};
+        if (!make_map(&ta1, w_uv, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&tx1, o, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLA_ERR_CUDA;
+    }
+    {   // out = W^O v : A K-major [128 d rows x 64 k], X = v [rows, H*d_h]
+        cuuint64_t ad[3] = {(cuuint64_t)K2, (cuuint64_t)d, 1};
+        cuuint64_t as[2] = {(cuuint64_t)K2 * 2, (cuuint64_t)K2 * d * 2};
+        cuuint32_t ab[3] = {64, 128, 1};
+        cuuint64_t xd[3] = {(cuuint64_t)K2, 1, (cuuint64_t)rows};
+        cuuint64_t xs[2] = {(cuuint64_t)K2 * 2, (cuuint64_t)K2 * 2};
+        cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g2.BN};
+        if (!make_map(&ta2, w_o, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&tx2, v_tmp, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLA_ERR_CUDA;
+    }
+    mla_status_t s = launch_gemm(ta1, tx1, d_h, rows, d_c, H, 0, 1, g1,
+                                 static_cast<__nv_bfloat16*>(v_tmp), (int64_t)K2, d_h, nullptr,
+                                 nullptr, st);
+    if (s != MLA_OK) return s;
+    float* ws_part = static_cast<float*>(workspace);
+    int* ws_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + part_bytes);
+    return launch_gemm(ta2, tx2, d, rows, K2, 1, 0, 0, g2, static_cast<__nv_bfloat16*>(out), d, 0,
+                       g2.splits > 1 ? ws_part : nullptr, g2.splits > 1 ? ws_count : nullptr, st);
+}
+
+// ---------------------------------------------------------- mla_combine
+
+mla_status_t mla_combine_splits(const float* o_part, const float* lse_part, int S, int64_t rows,
+                                int d_c, void* o, float* lse, mla_dtype_t dtype,
+                                mla_stream_t stream) {
+    if (!o_part || !lse_part || !o || !lse || S < 1 || S > 1024 || rows < 1 || d_c < 4 ||
+        d_c % 4 != 0)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o_part) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const unsigned blocks = (unsigned)((rows + 3) / 4);
+    if (dtype == MLA_FP32)
+        mla::combine_kernel<float><<<blocks, 128, 0, st>>>(o_part, lse_part, S, rows, d_c,
+                                                           static_cast<float*>(o), lse);
+    else if (dtype == MLA_BF16)
+        mla::combine_kernel<__nv_bfloat16><<<blocks, 128, 0, st>>>(
+            o_part, lse_part, S, rows, d_c, static_cast<__nv_bfloat16*>(o), lse);
+    else
+        return MLA_ERR_INVALID_ARG;
+    return launch_status();
+}
+
+// ------------------------------------------------------------ mla_decode
+
+size_t mla_decode_workspace_size(int B, int T, int H, int d_c, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || B < 1 || T < 1 || H < 1 || d_c < 1) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    const int64_t HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
+    return decode_ws_layout((int64_t)B * T * HG, di.decode_clusters, d_c).total;
+}
+
+mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv_pool,
+                             const int32_t* page_table, const int32_t* seq_lens,
+                             const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                             int d_r, int page_size, int max_pages, int64_t num_pages,
+                             float scale, int causal, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream) {
+    if (!q_lat || !q_pe || !kv_pool || !page_table || !seq_lens || !o || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (B < 1 || T < 1 || H < 1 || d_c < 1 || d_r < 0 || page_size < 1 || max_pages < 1 ||
+        num_pages < 1 || !std::isfinite(scale))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_lat) || !aligned16(q_pe) || !aligned16(kv_pool) || !aligned16(o))
+        return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == MLA_FP32) {
+        if (d_c > mla::FP32_MAX_DC || d_r > mla::FP32_MAX_DR || d_c % 4 != 0)
+            return MLA_ERR_UNSUPPORTED;
+        dim3 grid((unsigned)B * T, (unsigned)H);
+        mla::decode_fp32_kernel<<<grid, mla::FP32_WARPS * 32, 0, st>>>(
+            static_cast<const float*>(q_lat), static_cast<const float*>(q_pe),
+            static_cast<const float*>(kv_pool), page_table, seq_lens, T, H, d_c, d_r, page_size,
+            max_pages, num_pages, scale, causal ? 1 : 0, static_cast<float*>(o), lse);
+        return launch_status();
+    }
+    if (dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (d_c != mla::dec::DC || d_r != mla::dec::DR || page_size != mla::dec::PAGE)
+        return MLA_ERR_UNSUPPORTED;
+    if (num_pages * mla::dec::PAGE > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const int HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
+    const int64_t U = (int64_t)B * T * HG;
+    const int64_t G = di.decode_clusters;
+    const DecodeWs wl = decode_ws_layout(U, G, d_c);
+    if (!workspace || workspace_bytes < wl.total || !aligned16(workspace))
+        return MLA_ERR_INVALID_ARG;
+
+    CUtensorMap tm_c, tm_r;
+    const cuuint64_t dims[2] = {(cuuint64_t)(d_c + d_r), (cuuint64_t)num_pages * page_size};
+    const cuuint64_t strides[1] = {(cuuint64_t)(d_c + d_r) * 2};
+    const cuuint32_t box_c[2] = {64, (cuuint32_t)page_size};
+    const cuuint32_t box_r[2] = {(cuuint32_t)mla::dec::HALF_R, (cuuint32_t)page_size};
+    if (!make_map(&tm_c, kv_pool, 2, dims, strides, box_c, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_r, kv_pool, 2, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
+        return MLA_ERR_CUDA;
+
+    Params p;
+    p.q_lat = static_cast<const __nv_bfloat16*>(q_lat);
+    p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    p.page_table = page_table;
+    p.seq_lens = seq_lens;
+    p.o = static_cast<__nv_bfloat16*>(o);
+    p.lse = lse;
+    char* ws = static_cast<char*>(workspace);
+    p.ws_unit = reinterpret_cast<int2*>(ws + wl.unit_off);
+    p.ws_lse = reinterpret_cast<float*>(ws + wl.lse_off);
+    p.ws_o = reinterpret_cast<float*>(ws + wl.o_off);
+    p.B = B;
+    p.T = T;
+    p.H = H;
+    p.HG = HG;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.scale_log2 = scale * mla::dec::LOG2E;
+    p.causal = causal ? 1 : 0;
+
+    cudaEvent_t ev0 = g_ev_start, ev1 = g_ev_end;
+    if (ev0 && ev1 && cudaEventRecord(ev0, st) != cudaSuccess) return MLA_ERR_CUDA;
+    mla::dec::decode_bf16_kernel<<<(unsigned)(2 * G), mla::dec::THREADS, mla::dec::SMEM_ALLOC, st>>>(
+        tm_c, tm_r, p);
+    if (launch_status() != MLA_OK) return MLA_ERR_CUDA;
+    if (ev0 && ev1 && cudaEventRecord(ev1, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (seq_lens_host &&
+        !host_plan_needs_combine(seq_lens_host, B, T, HG, max_pages, p.causal, G))
+        return MLA_OK;
+    mla::dec::decode_combine_kernel<<<(unsigned)(U * mla::dec::HEADS), 128, 0, st>>>(p);
+    return launch_status();
+}
+
+}  // extern "C"

@@ -1,0 +1,35 @@
+// status.cuh -- the device status word shared by every kernel of the library.
+//
+// Kernels never trap, assert or spin forever.  A bounded wait that gives up,
+// or an out-of-range page id / sequence length found on the device, raises
+// the status word (first error wins) and the kernel winds down.  While the
+// word is raised, later kernels of this library on the same device return
+// early; mla_get_device_status() reads and clears it.
+#pragma once
+
+#include <cstdint>
+
+namespace mla {
+
+// Device-side error kinds (low 8 bits of the word); bits 8..31 hold a detail.
+enum : uint32_t {
+    MLA_DEV_OK = 0,
+    MLA_DEV_TIMEOUT = 1,
+    MLA_DEV_BOUNDS = 2,
+};
+
+// A bounded wait gives up after this much wall time (globaltimer, ns).
+constexpr uint64_t MLA_WAIT_LIMIT_NS = 2000000000ull;
+
+// Defined once: the library is a single translation unit (mla_lib.cu).
+__device__ uint32_t g_device_status = 0u;
+
+__device__ __forceinline__ bool device_status_raised() {
+    return *reinterpret_cast<volatile uint32_t*>(&g_device_status) != 0u;
+}
+
+__device__ __forceinline__ void raise_device_status(uint32_t kind, uint32_t detail) {
+    atomicCAS(&g_device_status, 0u, (kind & 0xFFu) | (detail << 8));
+}
+
+}  // namespace mla

@@ -1,0 +1,208 @@
+"""ctypes binding of libmla (include/mla.h): argument marshalling only.
+
+Every function takes CUDA torch tensors, passes their device pointers, sizes
+and the current stream to the C entry point of the same name, and raises
+``MLAError`` on a non-OK status.  Outputs and workspaces not supplied by the
+caller are allocated with torch (the library itself allocates nothing).
+There is no CPU path: if the library cannot be loaded, importing a function
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmla.so")
+
+MLA_BF16, MLA_FP32 = 0, 1
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
+          4: "MLA_ERR_TIMEOUT", 5: "MLA_ERR_DEVICE_BOUNDS"}
+
+SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_combine_splits",
+           "mla_out_proj_workspace_size", "mla_out_proj", "mla_get_device_status",
+           "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count"]
+
+
+class MLAError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn}: {STATUS.get(code, code)} ({_lib().mla_status_string(code).decode()})")
+
+
+_LIB = None
+
+
+def _lib():
+    """Load libmla.so (building it in-tree first if it is missing or stale)."""
+    global _LIB
+    if _LIB is None:
+        from . import build
+        if build.stale():
+            build.build()
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I, L, F, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                         ctypes.c_size_t)
+        lib.mla_absorb_q.argtypes = [P, P, P, I, I, I, I, I, P]
+        lib.mla_absorb_q.restype = I
+        lib.mla_decode_workspace_size.argtypes = [I, I, I, I, I]
+        lib.mla_decode_workspace_size.restype = Z
+        lib.mla_decode_attn.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, L, F, I, P, P, P, Z,
+                                        I, P]
+        lib.mla_decode_attn.restype = I
+        lib.mla_combine_splits.argtypes = [P, P, I, L, I, P, P, I, P]
+        lib.mla_combine_splits.restype = I
+        lib.mla_out_proj_workspace_size.argtypes = [I, I, I, I, I]
+        lib.mla_out_proj_workspace_size.restype = Z
+        lib.mla_out_proj.argtypes = [P, P, P, P, P, I, I, I, I, I, P, Z, I, P]
+        lib.mla_out_proj.restype = I
+        lib.mla_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.mla_get_device_status.restype = I
+        lib.mla_status_string.argtypes = [I]
+        lib.mla_status_string.restype = ctypes.c_char_p
+        lib.mla_version.argtypes = []
+        lib.mla_version.restype = I
+        lib.mla_set_decode_events.argtypes = [P, P]
+        lib.mla_set_decode_events.restype = None
+        lib.mla_launch_count.argtypes = []
+        lib.mla_launch_count.restype = ctypes.c_uint64
+        _LIB = lib
+    return _LIB
+
+
+def library():
+    """The loaded ctypes library handle."""
+    return _lib()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return MLA_BF16
+    if t.dtype == torch.float32:
+        return MLA_FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libmla takes CUDA tensors")
+    if not t.is_contiguous():
+        raise ValueError("libmla takes contiguous tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, code: int):
+    if code != 0:
+        raise MLAError(fn, code)
+
+
+# ------------------------------------------------------------------- entries
+
+def absorb_q(q_nope: torch.Tensor, w_uk: torch.Tensor, q_lat: torch.Tensor | None = None,
+             stream=None) -> torch.Tensor:
+    """q_lat[r,i,:] = W^UK_i^T q_nope[r,i,:]; q_nope [rows,H,d_h], w_uk [H,d_h,d_c]."""
+    rows, H, d_h = q_nope.shape
+    d_c = w_uk.shape[2]
+    if q_lat is None:
+        q_lat = torch.empty((rows, H, d_c), dtype=q_nope.dtype, device=q_nope.device)
+    _check("mla_absorb_q", _lib().mla_absorb_q(_ptr(q_nope), _ptr(w_uk), _ptr(q_lat), rows, H, d_h,
+                                               d_c, _dt(q_nope), _stream(stream)))
+    return q_lat
+
+
+def decode_workspace_size(B: int, T: int, H: int, d_c: int, dtype=torch.bfloat16) -> int:
+    return int(_lib().mla_decode_workspace_size(B, T, H, d_c,
+                                                MLA_BF16 if dtype == torch.bfloat16 else MLA_FP32))
+
+
+def decode_attn(q_lat, q_pe, kv_pool, page_table, seq_lens, scale: float, causal: bool = False,
+                o=None, lse=None, workspace=None, seq_lens_host=None, stream=None):
+    """Paged absorbed decode; returns (o [B,T,H,d_c], lse [B,T,H] fp32)."""
+    B, T, H, d_c = q_lat.shape
+    d_r = q_pe.shape[3]
+    num_pages, page, width = kv_pool.shape
+    max_pages = page_table.shape[1]
+    if o is None:
+        o = torch.empty_like(q_lat)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q_lat.device)
+    dt = _dt(q_lat)
+    need = int(_lib().mla_decode_workspace_size(B, T, H, d_c, dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
+    host = None
+    if seq_lens_host is not None:
+        seq_lens_host = seq_lens_host.to(torch.int32).contiguous()
+        host = ctypes.c_void_p(seq_lens_host.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_decode_attn", _lib().mla_decode_attn(
+        _ptr(q_lat), _ptr(q_pe), _ptr(kv_pool), _ptr(page_table), _ptr(seq_lens), host, B, T, H,
+        d_c, d_r, page, max_pages, num_pages, float(scale), int(bool(causal)), _ptr(o), _ptr(lse),
+        _ptr(workspace), ws_bytes, dt, _stream(stream)))
+    return o, lse
+
+
+def combine_splits(o_part, lse_part, o=None, lse=None, out_dtype=torch.bfloat16, stream=None):
+    """Merge [S, rows, d_c] fp32 partials and their [S, rows] lse; returns (o, lse)."""
+    S, rows, d_c = o_part.shape
+    if o is None:
+        o = torch.empty((rows, d_c), dtype=out_dtype, device=o_part.device)
+    if lse is None:
+        lse = torch.empty((rows,), dtype=torch.float32, device=o_part.device)
+    _check("mla_combine_splits", _lib().mla_combine_splits(
+        _ptr(o_part), _ptr(lse_part), S, rows, d_c, _ptr(o), _ptr(lse), _dt(o), _stream(stream)))
+    return o, lse
+
+
+def out_proj_workspace_size(rows: int, H: int, d_h: int, d: int, dtype=torch.bfloat16) -> int:
+    return int(_lib().mla_out_proj_workspace_size(
+        rows, H, d_h, d, MLA_BF16 if dtype == torch.bfloat16 else MLA_FP32))
+
+
+def out_proj(o, w_uv, w_o, v_tmp=None, out=None, workspace=None, stream=None):
+    """out = W^O concat_i(W^UV_i o_i); o [rows,H,d_c], w_uv [H,d_h,d_c], w_o [d,H*d_h]."""
+    rows, H, d_c = o.shape
+    d_h = w_uv.shape[1]
+    d = w_o.shape[0]
+    if v_tmp is None:
+        v_tmp = torch.empty((rows, H * d_h), dtype=o.dtype, device=o.device)
+    if out is None:
+        out = torch.empty((rows, d), dtype=o.dtype, device=o.device)
+    need = out_proj_workspace_size(rows, H, d_h, d, o.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=o.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_out_proj", _lib().mla_out_proj(
+        _ptr(o), _ptr(w_uv), _ptr(w_o), _ptr(v_tmp), _ptr(out), rows, H, d_h, d_c, d,
+        _ptr(workspace), ws_bytes, _dt(o), _stream(stream)))
+    return out
+
+
+def get_device_status(stream=None) -> tuple[int, int]:
+    """(status code, detail) of the current device; reads and clears the word."""
+    detail = ctypes.c_uint32(0)
+    code = _lib().mla_get_device_status(_stream(stream), ctypes.byref(detail))
+    return int(code), int(detail.value)
+
+
+def set_decode_events(start: torch.cuda.Event | None, end: torch.cuda.Event | None) -> None:
+    """Record `start`/`end` around the attention kernel of later bf16 decode calls."""
+    if start is None or end is None:
+        _lib().mla_set_decode_events(None, None)
+    else:
+        _lib().mla_set_decode_events(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(end.cuda_event))
+
+
+def launch_count() -> int:
+    """Kernels this library has launched in this process."""
+    return int(_lib().mla_launch_count())

@@ -1,0 +1,63 @@
+"""The C ABI library loads, exports every symbol the header declares, and
+rejects bad arguments on the host before touching a GPU (runs without one)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from mla_latent_kv_71_b300 import mla
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "mla.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ["mla_absorb_q", "mla_decode_attn", "mla_combine_splits", "mla_out_proj"]:
+        assert n in names
+    assert set(names) == set(mla.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    lib = mla.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings_and_version():
+    lib = mla.library()
+    assert lib.mla_version() >= 100
+    for code in range(6):
+        assert lib.mla_status_string(code)
+    assert b"invalid" in lib.mla_status_string(1)
+
+
+@pytest.mark.parametrize("dtype", [mla.MLA_BF16, mla.MLA_FP32])
+def test_null_pointers_are_rejected_on_the_host(dtype):
+    lib = mla.library()
+    assert lib.mla_absorb_q(None, None, None, 1, 1, 128, 512, dtype, None) == 1
+    assert lib.mla_decode_attn(None, None, None, None, None, None, 1, 1, 128, 512, 64, 64, 1, 1,
+                               0.07, 0, None, None, None, 0, dtype, None) == 1
+    assert lib.mla_combine_splits(None, None, 1, 1, 512, None, None, dtype, None) == 1
+    assert lib.mla_out_proj(None, None, None, None, None, 1, 1, 128, 512, 128, None, 0, dtype,
+                            None) == 1
+
+
+def test_bad_sizes_are_rejected_on_the_host():
+    lib = mla.library()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
+    assert lib.mla_decode_attn(fake, fake, fake, fake, fake, None, 0, 1, 128, 512, 64, 64, 1, 1,
+                               0.07, 0, fake, fake, fake, 0, mla.MLA_BF16, None) == 1
+    assert lib.mla_combine_splits(fake, fake, 0, 1, 512, fake, fake, mla.MLA_BF16, None) == 1
+    assert lib.mla_combine_splits(fake, fake, 2, 1, 6, fake, fake, mla.MLA_BF16, None) == 1
+    misaligned = ctypes.c_void_p((1 << 20) + 2)
+    assert lib.mla_absorb_q(misaligned, fake, fake, 1, 1, 128, 512, mla.MLA_BF16, None) == 1

@@ -1,0 +1,303 @@
+"""CUDA path vs the fp64 oracle on identical seeded inputs (needs a B300).
+
+Every call goes through the C ABI (``mla_latent_kv_71_b300.mla``).
+Tolerances (bf16 storage, fp32 accumulation):
+    o   : max |o - o*| <= 2e-2  and  ||o - o*||_F / ||o*||_F <= 5e-3
+    lse : max |lse - lse*| <= 1e-3
+    fp32 mode: max abs error <= 1e-4 on o, lse and out.
+The same bars apply to the final projection output of the end-to-end cases.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_71_b300 import mla, workloads
+
+pytestmark = pytest.mark.gpu
+
+O_MAX, O_FRO, LSE_MAX, FP32_MAX = 2e-2, 5e-3, 1e-3, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mla.library()
+    yield
+    code, detail = mla.get_device_status()
+    assert code == 0, f"device status {code} detail {detail:#x}"
+
+
+def _to(case: workloads.DecodeCase, device):
+    return workloads.DecodeCase(case.q_lat.to(device), case.q_pe.to(device), case.pool.to(device),
+                                case.page_table.to(device), case.seq_lens.to(device), case.scale,
+                                case.causal, dict(case.extra))
+
+
+def _check_o_lse(o, lse, o_ref, lse_ref, what=""):
+    o = np.asarray(o.float().cpu() if isinstance(o, torch.Tensor) else o, dtype=np.float64)
+    lse = np.asarray(lse.float().cpu() if isinstance(lse, torch.Tensor) else lse, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64).reshape(o.shape)
+    lse_ref = np.asarray(lse_ref, dtype=np.float64).reshape(lse.shape)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: lse finiteness differs"
+    assert np.isfinite(o).all(), f"{what}: non-finite o"
+    err = np.abs(o - o_ref).max()
+    fro = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
+    lerr = np.abs(lse[fin] - lse_ref[fin]).max() if fin.any() else 0.0
+    assert err <= O_MAX, f"{what}: max |o - o*| = {err:.3e}"
+    assert fro <= O_FRO, f"{what}: rel Frobenius = {fro:.3e}"
+    assert lerr <= LSE_MAX, f"{what}: max |lse - lse*| = {lerr:.3e}"
+    return err, fro, lerr
+
+
+def _run_decode(case, **kw):
+    torch.cuda.synchronize()
+    o, lse = mla.decode_attn(case.q_lat, case.q_pe, case.pool, case.page_table, case.seq_lens,
+                             case.scale, causal=case.causal, **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def _oracle_decode(case, sel=None):
+    c = _to(case, "cpu")
+    return oracle.decode_attn(c.q_lat, c.q_pe, c.pool, c.page_table, c.seq_lens, c.scale,
+                              causal=c.causal, sel=sel)
+
+
+# ------------------------------------------------------------ fp32 mode
+
+def test_fp32_decode_tiny_shapes():
+    spec = workloads.WORKLOADS["tiny_fp32"]
+    case = workloads.decode_case(2, 1, spec["H"], spec["d_c"], spec["d_r"], spec["lens"],
+                                 seed=0, dtype=torch.float32, device="cuda", d_h=spec["d_h"])
+    o, lse = _run_decode(case)
+    o_ref, lse_ref = _oracle_decode(case)
+    assert np.abs(o.cpu().double().numpy() - o_ref).max() <= FP32_MAX
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= FP32_MAX
+
+
+def test_fp32_end_to_end_tiny_widths():
+    """absorb_q -> decode -> out_proj in fp32 at the tiny model's widths."""
+    B, H, d_h, d_c, d_r, d = 2, 8, 32, 64, 16, 256
+    case = workloads.decode_case(B, 1, H, d_c, d_r, [128, 77], page=16, seed=3,
+                                 dtype=torch.float32, device="cuda", d_h=d_h)
+    qn = workloads.q_nope(B, 1, H, d_h, seed=4, device="cuda", dtype=torch.float32)
+    w_uk, w_uv, w_o = workloads.projection_weights(H, d_h, d_c, d, seed=5, device="cuda",
+                                                   dtype=torch.float32)
+    q_lat = mla.absorb_q(qn.view(B, H, d_h), w_uk)
+    o, lse = mla.decode_attn(q_lat.view(B, 1, H, d_c), case.q_pe, case.pool, case.page_table,
+                             case.seq_lens, case.scale)
+    out = mla.out_proj(o.view(B, H, d_c), w_uv, w_o)
+    torch.cuda.synchronize()
+    cpu = _to(case, "cpu")
+    q_ref = oracle.absorb_q(qn.cpu().view(B, H, d_h), w_uk.cpu())
+    o_ref, lse_ref = oracle.decode_attn(q_ref.reshape(B, 1, H, d_c), cpu.q_pe, cpu.pool,
+                                        cpu.page_table, cpu.seq_lens, cpu.scale)
+    out_ref, _ = oracle.out_proj(o_ref.reshape(B, H, d_c), w_uv.cpu(), w_o.cpu())
+    assert np.abs(q_lat.cpu().double().numpy() - q_ref).max() <= FP32_MAX
+    assert np.abs(o.cpu().double().numpy() - o_ref).max() <= FP32_MAX
+    assert np.abs(lse.cpu().double().numpy() - lse_ref).max() <= FP32_MAX
+    assert np.abs(out.cpu().double().numpy() - out_ref).max() <= FP32_MAX
+
+
+# ------------------------------------------------------------ bf16 decode
+
+SMALL = [
+    # (B, T, H, lens) -- several pages, ragged tails, a 1-token sequence
+    (3, 1, 128, [1, 65, 200]),
+    (4, 1, 128, [64, 128, 640, 1000]),
+    (2, 2, 128, [2, 129]),          # two causal query tokens
+    (3, 1, 16, [33, 64, 300]),      # fewer heads than the tile
+    (2, 1, 200, [70, 130]),         # two head groups
+    (2, 3, 128, [3, 250]),          # three causal query tokens
+]
+
+
+@pytest.mark.parametrize("B,T,H,lens", SMALL, ids=[f"B{c[0]}T{c[1]}H{c[2]}" for c in SMALL])
+def test_bf16_decode_small(B, T, H, lens):
+    case = workloads.decode_case(B, T, H, 512, 64, lens, seed=11 + B + T + H, device="cuda")
+    o, lse = _run_decode(case)
+    o_ref, lse_ref = _oracle_decode(case)
+    _check_o_lse(o, lse, o_ref, lse_ref, f"B{B}T{T}H{H}")
+
+
+def test_bf16_decode_many_sequences_split_across_clusters():
+    """More pages than clusters: most sequences are cut between SMs and merged."""
+    lens = [int(x) for x in torch.randint(1, 3000, (24,), generator=torch.Generator().manual_seed(5))]
+    case = workloads.decode_case(24, 1, 128, 512, 64, lens, seed=21, device="cuda")
+    o, lse = _run_decode(case)
+    o_ref, lse_ref = _oracle_decode(case)
+    _check_o_lse(o, lse, o_ref, lse_ref, "many")
+    o2, lse2 = _run_decode(case, seq_lens_host=case.seq_lens.cpu())
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_bf16_decode_empty_sequence():
+    case = workloads.decode_case(3, 1, 128, 512, 64, [0, 70, 5], seed=22, device="cuda")
+    o, lse = _run_decode(case)
+    assert torch.isneginf(lse[0]).all() and (o[0] == 0).all()
+    o_ref, lse_ref = _oracle_decode(case)
+    _check_o_lse(o, lse, o_ref, lse_ref, "empty")
+
+
+def test_bf16_decode_ignores_nan_past_the_end():
+    """Rows past a sequence's length may hold NaN: they must not reach o."""
+    case = workloads.decode_case(2, 1, 128, 512, 64, [70, 5], seed=23, device="cuda")
+    o_ref, lse_ref = _oracle_decode(case)
+    page = case.pool.shape[1]
+    for b, n in enumerate([70, 5]):
+        last = int(case.page_table[b, (n - 1) // page])
+        case.pool[last, n % page:] = float("nan")
+    o, lse = _run_decode(case)
+    _check_o_lse(o, lse, o_ref, lse_ref, "nan-tail")
+
+
+def test_bf16_decode_page_permutation_is_bitwise_invariant():
+    case = workloads.decode_case(3, 1, 128, 512, 64, [100, 700, 64], seed=24, device="cuda")
+    o1, l1 = _run_decode(case)
+    P = case.pool.shape[0]
+    perm = torch.randperm(P, generator=torch.Generator().manual_seed(9))
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(P)
+    pool2 = case.pool[perm.cuda()].contiguous()
+    table2 = case.page_table.clone()
+    valid = table2 >= 0
+    table2[valid] = inv.cuda()[table2[valid].long()].to(torch.int32)
+    o2, l2 = mla.decode_attn(case.q_lat, case.q_pe, pool2, table2, case.seq_lens, case.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_bf16_decode_head_order_equivariance():
+    case = workloads.decode_case(2, 1, 128, 512, 64, [300, 90], seed=25, device="cuda")
+    o1, l1 = _run_decode(case)
+    perm = torch.randperm(128, generator=torch.Generator().manual_seed(2)).cuda()
+    o2, l2 = mla.decode_attn(case.q_lat[:, :, perm].contiguous(), case.q_pe[:, :, perm].contiguous(),
+                             case.pool, case.page_table, case.seq_lens, case.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[:, :, perm], o2) and torch.equal(l1[:, :, perm], l2)
+
+
+def test_bf16_decode_hot_rows_stress_rescaling():
+    """A few latent rows scaled by 8 make the running maximum jump late."""
+    case = workloads.decode_case(2, 1, 128, 512, 64, [2000, 900], seed=26, device="cuda",
+                                 hot_frac=0.01)
+    o, lse = _run_decode(case)
+    o_ref, lse_ref = _oracle_decode(case)
+    _check_o_lse(o, lse, o_ref, lse_ref, "hot")
+
+
+def test_bf16_decode_bad_page_id_raises_device_status():
+    case = workloads.decode_case(2, 1, 128, 512, 64, [100, 100], seed=27, device="cuda")
+    case.page_table[1, 0] = case.pool.shape[0] + 5
+    _run_decode(case)
+    code, _ = mla.get_device_status()
+    assert code == 5
+    case.page_table[1, 0] = 0
+    o, lse = _run_decode(case)  # the context is still usable
+    assert mla.get_device_status()[0] == 0
+    assert torch.isfinite(lse).all()
+
+
+# ----------------------------------------------------- combine, projections
+
+def test_combine_splits_matches_oracle():
+    g = torch.Generator(device="cuda").manual_seed(31)
+    S, rows, d_c = 3, 300, 512
+    o_part = torch.randn((S, rows, d_c), generator=g, device="cuda")
+    lse_part = torch.randn((S, rows), generator=g, device="cuda") * 3
+    lse_part[1, :10] = float("-inf")
+    lse_part[:, 20] = float("-inf")
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = mla.combine_splits(o_part, lse_part, out_dtype=dt)
+        torch.cuda.synchronize()
+        o_ref, lse_ref = oracle.combine(o_part.cpu().numpy(), lse_part.cpu().numpy())
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lse.cpu().numpy()), fin)
+        tol = FP32_MAX if dt == torch.float32 else O_MAX
+        assert np.abs(o.float().cpu().numpy() - o_ref).max() <= tol
+        assert np.abs(lse.cpu().numpy()[fin] - lse_ref[fin]).max() <= 1e-4
+
+
+@pytest.mark.parametrize("rows,H", [(64, 128), (64, 16), (5, 8), (300, 2)])
+def test_bf16_absorb_q(rows, H):
+    qn = workloads.q_nope(rows, 1, H, 128, seed=41, device="cuda").view(rows, H, 128)
+    w_uk, _, _ = workloads.projection_weights(H, 128, 512, 128, seed=42, device="cuda")
+    q_lat = mla.absorb_q(qn, w_uk)
+    torch.cuda.synchronize()
+    ref = oracle.absorb_q(qn.cpu(), w_uk.cpu())
+    got = q_lat.float().cpu().numpy()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= O_FRO and np.abs(got - ref).max() <= O_MAX * max(1.0, np.abs(ref).max())
+
+
+@pytest.mark.parametrize("rows,H,d", [(64, 128, 7168), (64, 16, 7168), (7, 4, 256)])
+def test_bf16_out_proj(rows, H, d):
+    g = torch.Generator(device="cuda").manual_seed(43)
+    o = (torch.randn((rows, H, 512), generator=g, device="cuda") * 0.05).to(torch.bfloat16)
+    _, w_uv, w_o = workloads.projection_weights(H, 128, 512, d, seed=44, device="cuda")
+    out = mla.out_proj(o, w_uv, w_o)
+    out2 = mla.out_proj(o, w_uv, w_o)  # counters of the split-K reduction are reusable
+    torch.cuda.synchronize()
+    ref, _ = oracle.out_proj(o.cpu(), w_uv.cpu(), w_o.cpu())
+    got = out.float().cpu().numpy()
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert rel <= O_FRO, rel
+    assert np.abs(got - ref).max() <= O_MAX
+    assert torch.equal(out, out2)
+
+
+# ----------------------------------------------- full-size workloads (sampled)
+
+def _sampled_check(case, n_rows=48, seed=0):
+    """GPU over the whole workload; oracle on sampled (b, t, head) rows."""
+    o, lse = _run_decode(case)
+    B, T, H, d_c = case.q_lat.shape
+    g = np.random.default_rng(seed)
+    sel = np.sort(g.choice(B * T * H, size=min(n_rows, B * T * H), replace=False))
+    o_ref, lse_ref = _oracle_decode(case, sel=sel)
+    o_got = o.reshape(-1, d_c)[torch.from_numpy(sel).cuda()]
+    l_got = lse.reshape(-1)[torch.from_numpy(sel).cuda()]
+    assert torch.isfinite(lse).all() and torch.isfinite(o.float()).all()
+    return _check_o_lse(o_got, l_got, o_ref, lse_ref, "sampled")
+
+
+@pytest.mark.parametrize("name", ["decode_b64_h128_l4096", "ragged_b128_l16k", "long_b4_l128k"])
+def test_full_size_workloads_sampled(name):
+    case = workloads.make_workload(name, device="cuda")
+    _sampled_check(case)
+
+
+@pytest.mark.parametrize("name", ["mtp_b32_t2_l8192", "smallhead_b64_h16_l32k"])
+def test_full_size_end_to_end_sampled(name):
+    """absorb_q -> decode -> out_proj at full size; oracle on sampled sequences."""
+    case = workloads.make_workload(name, device="cuda")
+    B, T, H, d_c = case.q_lat.shape
+    qn = case.extra["q_nope"]
+    w_uk, w_uv, w_o = case.extra["w_uk"], case.extra["w_uv"], case.extra["w_o"]
+    q_lat = mla.absorb_q(qn.view(B * T, H, -1), w_uk).view(B, T, H, d_c)
+    o, lse = mla.decode_attn(q_lat, case.q_pe, case.pool, case.page_table, case.seq_lens,
+                             case.scale, causal=case.causal)
+    out = mla.out_proj(o.view(B * T, H, d_c), w_uv, w_o)
+    torch.cuda.synchronize()
+    # oracle on two sequences: fp64 absorb from the same bf16 q_nope
+    bs = [0, B - 1]
+    sub = workloads.DecodeCase(q_lat[bs], case.q_pe[bs], case.pool, case.page_table[bs],
+                               case.seq_lens[bs], case.scale, case.causal)
+    cpu = _to(sub, "cpu")
+    q_ref = oracle.absorb_q(qn[bs].cpu().reshape(len(bs) * T, H, -1), w_uk.cpu())
+    o_ref, lse_ref = oracle.decode_attn(q_ref.reshape(len(bs), T, H, d_c), cpu.q_pe, cpu.pool,
+                                        cpu.page_table, cpu.seq_lens, cpu.scale, causal=cpu.causal)
+    out_ref, _ = oracle.out_proj(o_ref.reshape(len(bs) * T, H, d_c), w_uv.cpu(), w_o.cpu())
+    _check_o_lse(o[bs], lse[bs], o_ref, lse_ref, name)
+    got = out.view(B, T, -1)[bs].float().cpu().numpy().reshape(out_ref.shape)
+    rel = np.linalg.norm(got - out_ref) / np.linalg.norm(out_ref)
+    assert rel <= O_FRO, rel
+    assert np.abs(got - out_ref).max() <= O_MAX
