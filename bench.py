@@ -89,6 +89,7 @@ class ClockSampler:
 
     def __init__(self, device_index: int):
         self.samples, self.reasons, self.ok = [], set(), False
+        self.err = ""
         self.max_mhz = None
         try:
             import pynvml
@@ -103,6 +104,7 @@ class ClockSampler:
             self.ok = True
         except Exception as e:  # pragma: no cover - no NVML
             self.err = repr(e)
+            self.ok = False
         self._stop = threading.Event()
 
     def _run(self):
@@ -113,8 +115,8 @@ class ClockSampler:
                 for name, bit in self.REASONS.items():
                     if mask & bit:
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.err = repr(e)
             time.sleep(0.002)
 
     def __enter__(self):
@@ -131,7 +133,7 @@ class ClockSampler:
     def summary(self):
         if not self.ok or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "note": "no NVML samples"}
+                    "note": "no NVML samples: " + getattr(self, "err", "")}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
                 "reasons": sorted(self.reasons), "samples": len(self.samples)}
 
@@ -258,6 +260,10 @@ def run_ours(args, rank, world, local):
 
     ev_attn = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(args.steps)]
+    for a, b in ev_attn:  # torch creates events lazily: record once so the handles exist
+        a.record(s)
+        b.record(s)
+    torch.cuda.synchronize(dev)
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     barrier(world)

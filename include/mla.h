@@ -128,6 +128,24 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
                              size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
 
 /*
+ * mla_decode_plan -- how mla_decode_attn (bf16) divides a batch over the GPU,
+ * computed on the host from the same arithmetic the kernel uses.
+ * The pages of all units u = (b*T + t)*ceil(H/128) + head_group are laid end
+ * to end and cut into min(clusters, total pages) equal contiguous ranges, one
+ * per 2-CTA cluster; a unit cut by a range boundary is computed in pieces
+ * whose partial results are merged by log-sum-exp.
+ *   seq_lens_host [B] int32 (host), clusters: co-resident clusters (0 = the
+ *   current device's value).
+ *   out: up to `cap` rows of 7 int64: (cluster, unit, first page, end page
+ *   (exclusive, within the unit), partial slot or -1 when the unit is whole,
+ *   cluster of the unit's first page, cluster of its last page).
+ * Returns the number of pieces (which may exceed cap), or -1 on bad
+ * arguments.  Units that see no position produce no piece.
+ */
+int64_t mla_decode_plan(const int32_t* seq_lens_host, int B, int T, int H, int max_pages,
+                        int causal, int clusters, int64_t* out, int64_t cap);
+
+/*
  * mla_combine_splits -- merge S partial results of the same softmax rows,
  * each computed over a disjoint subset of the cached positions:
  *     lse = ln sum_s exp(lse_part[s]),   o = sum_s exp(lse_part[s] - lse) o_part[s]

@@ -104,68 +104,90 @@ struct Params {
     int causal;
 };
 
-// Visible positions and pages of unit u = ((b*T + t)*HG + hg).
+// ------------------------------------------------------------------ plan
+//
+// The work plan is a pure function of the sequence lengths, shared by the
+// kernel (every CTA derives it independently) and by the host
+// (mla_decode_plan, and the decision to skip the combine launch).
+//
+// Units u = ((b*T + t)*HG + hg) are laid end to end by their pages; the line
+// of `total` pages is cut into G = min(clusters, total) contiguous ranges,
+// range g = [total*g/G, total*(g+1)/G), none of them empty.  A unit cut by a
+// range boundary is processed in pieces; piece (g, u) writes partial slot
+// g + u, which is unique because both g and u only grow along the line.
+
+struct PlanView {
+    const int32_t* seq_lens;  // [B]
+    int B, T, HG, max_pages, causal;
+};
+
+// Visible positions and pages of unit u.
 struct Unit {
     int b, t, hg;
     int64_t len;    // visible positions
     int64_t pages;  // ceil(len / 64)
+    bool bad_len;   // seq_lens[b] outside [0, max_pages * 64] (clamped)
 };
 
-__device__ __forceinline__ Unit unit_of(const Params& p, int64_t u) {
+__host__ __device__ __forceinline__ Unit unit_of(const PlanView& v, int64_t u) {
     Unit r;
-    const int64_t bt = u / p.HG;
-    r.hg = (int)(u % p.HG);
-    r.b = (int)(bt / p.T);
-    r.t = (int)(bt % p.T);
-    int64_t len = p.seq_lens[r.b];
-    const int64_t cap = (int64_t)p.max_pages * PAGE;
-    if (len < 0 || len > cap) {
-        raise_device_status(MLA_DEV_BOUNDS, 0x10);
-        len = len < 0 ? 0 : cap;
-    }
-    int64_t n = p.causal ? len - (p.T - 1 - r.t) : len;
+    const int64_t bt = u / v.HG;
+    r.hg = (int)(u % v.HG);
+    r.b = (int)(bt / v.T);
+    r.t = (int)(bt % v.T);
+    int64_t len = v.seq_lens[r.b];
+    const int64_t cap = (int64_t)v.max_pages * PAGE;
+    r.bad_len = len < 0 || len > cap;
+    if (r.bad_len) len = len < 0 ? 0 : cap;
+    const int64_t n = v.causal ? len - (v.T - 1 - r.t) : len;
     r.len = n < 0 ? 0 : n;
     r.pages = (r.len + PAGE - 1) / PAGE;
     return r;
 }
 
-// Range [rs, re) of the page line owned by cluster g of G.
-__device__ __forceinline__ int64_t range_start(int64_t total, int64_t g, int64_t G) {
+__host__ __device__ __forceinline__ int64_t range_start(int64_t total, int64_t g, int64_t G) {
     return total * g / G;
 }
 
-__device__ __forceinline__ int64_t cluster_of_page(int64_t x, int64_t total, int64_t G) {
+// Clusters used for `total` pages when `launched` clusters run.
+__host__ __device__ __forceinline__ int64_t clusters_used(int64_t total, int64_t launched) {
+    return total < launched ? total : launched;
+}
+
+// The range (cluster) holding page x of the line.
+__host__ __device__ __forceinline__ int64_t cluster_of_page(int64_t x, int64_t total, int64_t G) {
     int64_t g = x * G / total;
     while (g + 1 < G && range_start(total, g + 1, G) <= x) ++g;
     while (g > 0 && range_start(total, g, G) > x) --g;
     return g;
 }
 
-// A piece of a unit processed by this cluster.
+// A piece of a unit processed by one cluster.
 struct Segment {
     int64_t u;
     Unit un;
-    int64_t lp0, lp1;  // local page range within the unit
-    int64_t slot;      // partial slot, or -1 when the whole unit is here
-    int64_t g_first, g_last;
+    int64_t lp0, lp1;          // page range within the unit
+    int64_t slot;              // partial slot, or -1 when the whole unit is here
+    int64_t g_first, g_last;   // clusters holding the unit's first and last page
 };
 
-// Walks the units overlapping [rs, re) in order.
+// Walks the units overlapping cluster g's range, in line order.
 struct Walker {
-    const Params* p;
+    PlanView v;
     int64_t U, rs, re, total, G, g;
-    int64_t u, pos;  // next unit, its first page on the line
-    __device__ bool next(Segment& s) {
+    int64_t u, pos;  // next unit and its first page on the line
+    __host__ __device__ bool next(Segment& s) {
+        if (rs >= re) return false;  // an empty range has no piece
         while (pos < re && u < U) {
-            const Unit un = unit_of(*p, u);
+            const Unit un = unit_of(v, u);
             const int64_t start = pos;
             pos += un.pages;
             const int64_t cu = u++;
             if (un.pages == 0 || pos <= rs) continue;
             s.u = cu;
             s.un = un;
-            s.lp0 = max(rs, start) - start;
-            s.lp1 = min(re, pos) - start;
+            s.lp0 = (rs > start ? rs : start) - start;
+            s.lp1 = (re < pos ? re : pos) - start;
             s.g_first = cluster_of_page(start, total, G);
             s.g_last = cluster_of_page(pos - 1, total, G);
             s.slot = (s.g_first == s.g_last) ? -1 : g + cu;
@@ -174,6 +196,35 @@ struct Walker {
         return false;
     }
 };
+
+// Walker of cluster g, found by a sequential scan (host side).
+inline Walker host_walker(const PlanView& v, int64_t launched, int64_t g) {
+    Walker w;
+    w.v = v;
+    w.U = (int64_t)v.B * v.T * v.HG;
+    int64_t total = 0;
+    for (int64_t u = 0; u < w.U; ++u) total += unit_of(v, u).pages;
+    w.total = total;
+    w.G = clusters_used(total, launched);
+    w.g = g;
+    w.rs = w.re = 0;
+    w.u = w.U;
+    w.pos = 0;
+    if (total == 0 || g >= w.G) return w;
+    w.rs = range_start(total, g, w.G);
+    w.re = range_start(total, g + 1, w.G);
+    int64_t pos = 0;
+    for (int64_t u = 0; u < w.U; ++u) {
+        const int64_t n = unit_of(v, u).pages;
+        if (w.rs < pos + n) {
+            w.u = u;
+            w.pos = pos;
+            break;
+        }
+        pos += n;
+    }
+    return w;
+}
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_r,
@@ -227,12 +278,26 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 
     // ---------------------------------------------------------------- plan
     // Every CTA derives the same cut of the page line from seq_lens.
+    PlanView pv;
+    pv.seq_lens = p.seq_lens;
+    pv.B = p.B;
+    pv.T = p.T;
+    pv.HG = p.HG;
+    pv.max_pages = p.max_pages;
+    pv.causal = p.causal;
     const int64_t U = (int64_t)p.B * p.T * p.HG;
+    const int64_t launched = num_clusters_x(), g_id = cluster_id_x();
     {
         const int64_t chunk = (U + THREADS - 1) / THREADS;
         const int64_t u0 = min(U, (int64_t)threadIdx.x * chunk), u1 = min(U, u0 + chunk);
         int64_t sum = 0;
-        for (int64_t u = u0; u < u1; ++u) sum += unit_of(p, u).pages;
+        bool bad = false;
+        for (int64_t u = u0; u < u1; ++u) {
+            const Unit un = unit_of(pv, u);
+            sum += un.pages;
+            bad |= un.bad_len;
+        }
+        if (bad && rank == 0 && g_id == 0) raise_device_status(MLA_DEV_BOUNDS, 0x10);
         scan[threadIdx.x] = sum;
         __syncthreads();
         if (threadIdx.x == 0) {
@@ -249,13 +314,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         }
         __syncthreads();
         const int64_t total = misc[0];
-        const int64_t G = num_clusters_x(), g = cluster_id_x();
-        const int64_t rs = total > 0 ? range_start(total, g, G) : 0;
+        const int64_t G = clusters_used(total, launched);
+        const int64_t rs = g_id < G ? range_start(total, g_id, G) : total;
         const int64_t pre = scan[threadIdx.x];
-        if (total > 0 && rs >= pre && rs < pre + sum) {
+        if (g_id < G && rs >= pre && rs < pre + sum) {
             int64_t pos = pre;
             for (int64_t u = u0; u < u1; ++u) {
-                const int64_t n = unit_of(p, u).pages;
+                const int64_t n = unit_of(pv, u).pages;
                 if (rs < pos + n) {
                     misc[1] = u;
                     misc[2] = pos;
@@ -272,13 +337,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 
     const uint32_t tmem = *tmem_slot;
     Walker walk;
-    walk.p = &p;
+    walk.v = pv;
     walk.U = U;
     walk.total = misc[0];
-    walk.G = num_clusters_x();
-    walk.g = cluster_id_x();
-    walk.rs = walk.total > 0 ? range_start(walk.total, walk.g, walk.G) : 0;
-    walk.re = walk.total > 0 ? range_start(walk.total, walk.g + 1, walk.G) : 0;
+    walk.G = clusters_used(walk.total, launched);
+    walk.g = g_id;
+    walk.rs = g_id < walk.G ? range_start(walk.total, g_id, walk.G) : 0;
+    walk.re = g_id < walk.G ? range_start(walk.total, g_id + 1, walk.G) : 0;
     walk.u = misc[1];
     walk.pos = misc[2];
     const bool skip = misc[3] != 0;
@@ -617,7 +682,14 @@ decode_combine_kernel(const Params p) {
     if (device_status_raised()) return;
     const int64_t u = blockIdx.x / HEADS;
     const int h = blockIdx.x % HEADS;
-    const Unit un = unit_of(p, u);
+    PlanView pv;
+    pv.seq_lens = p.seq_lens;
+    pv.B = p.B;
+    pv.T = p.T;
+    pv.HG = p.HG;
+    pv.max_pages = p.max_pages;
+    pv.causal = p.causal;
+    const Unit un = unit_of(pv, u);
     const int head = un.hg * HEADS + h;
     if (head >= p.H) return;
     const int64_t qrow = ((int64_t)un.b * p.T + un.t) * p.H + head;

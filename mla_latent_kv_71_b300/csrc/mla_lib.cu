@@ -126,34 +126,24 @@ mla_status_t launch_status(int n = 1) {
 
 // ------------------------------------------------------------ decode plan
 
-// Host copy of the kernel's range arithmetic: does any unit straddle two
-// clusters (or see no position)?  Used only to skip the combine launch.
+// Does the plan cut some unit between clusters, or leave one without any
+// visible position?  (Only then is the combine kernel needed.)
 bool host_plan_needs_combine(const int32_t* lens, int B, int T, int HG, int max_pages, int causal,
-                             int64_t G) {
-    std::vector<int64_t> pages;
-    pages.reserve((size_t)B * T * HG);
+                             int64_t launched) {
+    mla::dec::PlanView v{lens, B, T, HG, max_pages, causal};
+    const int64_t U = (int64_t)B * T * HG;
     int64_t total = 0;
-    for (int b = 0; b < B; ++b) {
-        int64_t len = lens[b];
-        if (len < 0 || len > (int64_t)max_pages * 64) return true;
-        for (int t = 0; t < T; ++t) {
-            int64_t n = causal ? len - (T - 1 - t) : len;
-            if (n <= 0) return true;
-            for (int hg = 0; hg < HG; ++hg) {
-                pages.push_back((n + 63) / 64);
-                total += (n + 63) / 64;
-            }
-        }
+    for (int64_t u = 0; u < U; ++u) {
+        const mla::dec::Unit un = mla::dec::unit_of(v, u);
+        if (un.pages == 0 || un.bad_len) return true;
+        total += un.pages;
     }
-    auto cl = [&](int64_t x) {
-        int64_t g = x * G / total;
-        while (g + 1 < G && total * (g + 1) / G <= x) ++g;
-        while (g > 0 && total * g / G > x) --g;
-        return g;
-    };
+    const int64_t G = mla::dec::clusters_used(total, launched);
     int64_t pos = 0;
-    for (int64_t n : pages) {
-        if (cl(pos) != cl(pos + n - 1)) return true;
+    for (int64_t u = 0; u < U; ++u) {
+        const int64_t n = mla::dec::unit_of(v, u).pages;
+        if (mla::dec::cluster_of_page(pos, total, G) != mla::dec::cluster_of_page(pos + n - 1, total, G))
+            return true;
         pos += n;
     }
     return false;
@@ -407,6 +397,39 @@ size_t mla_decode_workspace_size(int B, int T, int H, int d_c, mla_dtype_t dtype
     if (!device_info(di)) return 0;
     const int64_t HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
     return decode_ws_layout((int64_t)B * T * HG, di.decode_clusters, d_c).total;
+}
+
+int64_t mla_decode_plan(const int32_t* seq_lens_host, int B, int T, int H, int max_pages,
+                        int causal, int clusters, int64_t* out, int64_t cap) {
+    if (!seq_lens_host || B < 1 || T < 1 || H < 1 || max_pages < 1 || clusters < 0 || cap < 0 ||
+        (cap > 0 && !out))
+        return -1;
+    if (clusters == 0) {
+        DeviceInfo di;
+        if (!device_info(di)) return -1;
+        clusters = di.decode_clusters;
+    }
+    const int HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
+    mla::dec::PlanView v{seq_lens_host, B, T, HG, max_pages, causal ? 1 : 0};
+    int64_t n = 0;
+    for (int64_t g = 0; g < clusters; ++g) {
+        mla::dec::Walker w = mla::dec::host_walker(v, clusters, g);
+        mla::dec::Segment sg;
+        while (w.next(sg)) {
+            if (n < cap) {
+                int64_t* r = out + 7 * n;
+                r[0] = g;
+                r[1] = sg.u;
+                r[2] = sg.lp0;
+                r[3] = sg.lp1;
+                r[4] = sg.slot;
+                r[5] = sg.g_first;
+                r[6] = sg.g_last;
+            }
+            ++n;
+        }
+    }
+    return n;
 }
 
 mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv_pool,

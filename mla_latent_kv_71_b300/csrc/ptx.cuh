@@ -91,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
             return true;
         if (device_status_raised()) return false;
         if (global_timer_ns() - t0 > MLA_WAIT_LIMIT_NS) {
-            raise_device_status(MLA_DEV_TIMEOUT, where);
+            raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
             return false;
         }
     }

@@ -24,7 +24,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 
 SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_combine_splits",
            "mla_out_proj_workspace_size", "mla_out_proj", "mla_get_device_status",
-           "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count"]
+           "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count",
+           "mla_decode_plan"]
 
 
 class MLAError(RuntimeError):
@@ -69,6 +70,8 @@ def _lib():
         lib.mla_set_decode_events.restype = None
         lib.mla_launch_count.argtypes = []
         lib.mla_launch_count.restype = ctypes.c_uint64
+        lib.mla_decode_plan.argtypes = [P, I, I, I, I, I, I, P, L]
+        lib.mla_decode_plan.restype = L
         _LIB = lib
     return _LIB
 
@@ -206,3 +209,22 @@ def set_decode_events(start: torch.cuda.Event | None, end: torch.cuda.Event | No
 def launch_count() -> int:
     """Kernels this library has launched in this process."""
     return int(_lib().mla_launch_count())
+
+
+def decode_plan(seq_lens, T: int, H: int, max_pages: int, causal: bool = False,
+                clusters: int = 0):
+    """Pieces of the bf16 decode work split (host computation), as a list of
+    dicts with keys cluster, unit, lp0, lp1, slot, g_first, g_last."""
+    import numpy as np
+    lens = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32))
+    B = lens.shape[0]
+    lib = _lib()
+    n = lib.mla_decode_plan(lens.ctypes.data_as(ctypes.c_void_p), B, T, H, max_pages,
+                            int(bool(causal)), clusters, None, 0)
+    if n < 0:
+        raise ValueError("mla_decode_plan: bad arguments")
+    out = np.zeros((max(n, 1), 7), dtype=np.int64)
+    lib.mla_decode_plan(lens.ctypes.data_as(ctypes.c_void_p), B, T, H, max_pages,
+                        int(bool(causal)), clusters, out.ctypes.data_as(ctypes.c_void_p), n)
+    keys = ["cluster", "unit", "lp0", "lp1", "slot", "g_first", "g_last"]
+    return [dict(zip(keys, map(int, row))) for row in out[:n]]

@@ -2,10 +2,14 @@
 
 Every call goes through the C ABI (``mla_latent_kv_71_b300.mla``).
 Tolerances (bf16 storage, fp32 accumulation):
-    o   : max |o - o*| <= 2e-2  and  ||o - o*||_F / ||o*||_F <= 5e-3
+    o   : |o - o*| <= 2e-2 + 2^-8 |o*| elementwise, and
+          ||o - o*||_F / ||o*||_F <= 5e-3
     lse : max |lse - lse*| <= 1e-3
     fp32 mode: max abs error <= 1e-4 on o, lse and out.
-The same bars apply to the final projection output of the end-to-end cases.
+The absolute bar on o is 2e-2 plus half a bf16 unit in the last place of the
+reference value (2^-8 |o*| bounds it): where |o*| > 5, as when a few latent
+rows are 8x larger, rounding the output to bf16 alone exceeds 2e-2.  The
+same bars apply to the final projection output of the end-to-end cases.
 """
 
 from __future__ import annotations
@@ -22,6 +26,7 @@ from mla_latent_kv_71_b300 import mla, workloads
 pytestmark = pytest.mark.gpu
 
 O_MAX, O_FRO, LSE_MAX, FP32_MAX = 2e-2, 5e-3, 1e-3, 1e-4
+BF16_HALF_ULP = 2.0 ** -8  # relative bound on half a bf16 ulp
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -30,8 +35,15 @@ def _cuda():
         pytest.skip("no CUDA device")
     mla.library()
     yield
+
+
+@pytest.fixture(autouse=True)
+def _device_status():
+    """Each test starts with a clear device status word and must leave it clear."""
+    mla.get_device_status()
+    yield
     code, detail = mla.get_device_status()
-    assert code == 0, f"device status {code} detail {detail:#x}"
+    assert code == 0, f"device status {code}: site {detail & 0xFFF:#x} block {detail >> 12}"
 
 
 def _to(case: workloads.DecodeCase, device):
@@ -49,9 +61,10 @@ def _check_o_lse(o, lse, o_ref, lse_ref, what=""):
     assert np.array_equal(np.isfinite(lse), fin), f"{what}: lse finiteness differs"
     assert np.isfinite(o).all(), f"{what}: non-finite o"
     err = np.abs(o - o_ref).max()
+    excess = (np.abs(o - o_ref) - (O_MAX + BF16_HALF_ULP * np.abs(o_ref))).max()
     fro = np.linalg.norm(o - o_ref) / max(np.linalg.norm(o_ref), 1e-30)
     lerr = np.abs(lse[fin] - lse_ref[fin]).max() if fin.any() else 0.0
-    assert err <= O_MAX, f"{what}: max |o - o*| = {err:.3e}"
+    assert excess <= 0, f"{what}: max |o - o*| = {err:.3e} exceeds the bar by {excess:.3e}"
     assert fro <= O_FRO, f"{what}: rel Frobenius = {fro:.3e}"
     assert lerr <= LSE_MAX, f"{what}: max |lse - lse*| = {lerr:.3e}"
     return err, fro, lerr
@@ -287,17 +300,29 @@ def test_full_size_end_to_end_sampled(name):
                              case.scale, causal=case.causal)
     out = mla.out_proj(o.view(B * T, H, d_c), w_uv, w_o)
     torch.cuda.synchronize()
-    # oracle on two sequences: fp64 absorb from the same bf16 q_nope
+    # Oracle on two sequences.  Stage by stage on identical inputs: absorb
+    # from the bf16 q_nope, decode from the GPU's bf16 q_lat, out_proj from the
+    # GPU's o.  Then the fp64 chain from q_nope, compared on the final output
+    # (q_lat and o are stored in bf16 between the stages, which moves lse by
+    # up to a few 1e-3 for short sequences; the chain is judged on out).
     bs = [0, B - 1]
     sub = workloads.DecodeCase(q_lat[bs], case.q_pe[bs], case.pool, case.page_table[bs],
                                case.seq_lens[bs], case.scale, case.causal)
     cpu = _to(sub, "cpu")
     q_ref = oracle.absorb_q(qn[bs].cpu().reshape(len(bs) * T, H, -1), w_uk.cpu())
-    o_ref, lse_ref = oracle.decode_attn(q_ref.reshape(len(bs), T, H, d_c), cpu.q_pe, cpu.pool,
-                                        cpu.page_table, cpu.seq_lens, cpu.scale, causal=cpu.causal)
-    out_ref, _ = oracle.out_proj(o_ref.reshape(len(bs) * T, H, d_c), w_uv.cpu(), w_o.cpu())
+    q_got = q_lat[bs].float().cpu().numpy().reshape(q_ref.shape)
+    assert np.linalg.norm(q_got - q_ref) <= O_FRO * np.linalg.norm(q_ref)
+    o_ref, lse_ref = oracle.decode_attn(cpu.q_lat, cpu.q_pe, cpu.pool, cpu.page_table,
+                                        cpu.seq_lens, cpu.scale, causal=cpu.causal)
     _check_o_lse(o[bs], lse[bs], o_ref, lse_ref, name)
+    stage_ref, _ = oracle.out_proj(o[bs].cpu().reshape(len(bs) * T, H, d_c), w_uv.cpu(),
+                                   w_o.cpu())
+    got = out.view(B, T, -1)[bs].float().cpu().numpy().reshape(stage_ref.shape)
+    assert np.linalg.norm(got - stage_ref) <= O_FRO * np.linalg.norm(stage_ref)
+    o64, _ = oracle.decode_attn(q_ref.reshape(len(bs), T, H, d_c), cpu.q_pe, cpu.pool,
+                                cpu.page_table, cpu.seq_lens, cpu.scale, causal=cpu.causal)
+    out_ref, _ = oracle.out_proj(o64.reshape(len(bs) * T, H, d_c), w_uv.cpu(), w_o.cpu())
     got = out.view(B, T, -1)[bs].float().cpu().numpy().reshape(out_ref.shape)
     rel = np.linalg.norm(got - out_ref) / np.linalg.norm(out_ref)
     assert rel <= O_FRO, rel
-    assert np.abs(got - out_ref).max() <= O_MAX
+    assert (np.abs(got - out_ref) <= O_MAX + BF16_HALF_ULP * np.abs(out_ref)).all()
