@@ -409,6 +409,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         if (!ok) {  // let every issued copy land before the CTA can exit
             for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
                 mbar_wait(FULL((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), 0x203);
+        } else {
+            // Producer tail: the tensor core's last releases of the ring
+            // (tcgen05.commit arrivals) land before shared memory goes away.
+            for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
+                mbar_wait(EMPTY((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), 0x204);
         }
     } else if (warp == 1) {
         // ============================================================== MMA
