@@ -7,31 +7,50 @@
 // Key Absorption", "Value Output Absorption"; [Zhang] "Decoupled RoPE",
 // "Value absorption"; [Mishra] "Step 4: decoupled RoPE").  All heads of a
 // query share the cache rows, so the 128 heads form the M = 128 rows of two
-// dense UMMA contractions per 64-token page:
-//     S [128 x 64]  = Q [128 x 576] . K^T     (K = the page's 576-wide rows)
-//     O [128 x 512] += P [128 x 64] . C       (C = the page's 512 latents)
+// dense UMMA contractions per tile of 32 cached tokens:
+//     S [128 x 32]  = Q [128 x 576] . K^T     (K = the tile's 576-wide rows)
+//     O [128 x 512] += P [128 x 32] . C       (C = the tile's 512 latents)
 //
 // Layout on the chip.  O alone (128 x 512 fp32) fills a whole SM's TMEM, so
 // a cluster of two CTAs splits the feature axis: CTA r owns latent columns
 // 256r .. 256r+255 and RoPE columns 32r .. 32r+31 (288 of the 576 features).
-// Each CTA loads only its half of every page (36 KB, one TMA box per 64
-// columns), computes a partial S over its 288 features, and the two partial
-// S tiles are exchanged through distributed shared memory (st.async with
-// transaction-count completion).  Both CTAs then hold the identical full S,
-// run the identical online softmax and accumulate their own 256 columns of O.
-// Every cache byte is read from HBM once and no tensor work is duplicated.
+// Each CTA loads only its half of every 64-token page (36 KB: one TMA box
+// per 64 columns), computes a partial S over its 288 features, and the two
+// partial S tiles are exchanged through distributed shared memory.  Both
+// CTAs then run the identical softmax and accumulate their own 256 columns
+// of O.  Every cache byte is read from HBM once and no tensor work is
+// duplicated.
+//
+// The exchange (16 KB per tile each way) is slow next to the rest of a tile,
+// so it is pipelined: S and P are double-buffered in TMEM, and two groups of
+// four warps take alternate tiles.  Each group sends its partial S tile to
+// the peer (st.async from registers), receives the peer's, and runs the
+// softmax of its tile, so one tile's exchange overlaps the other's
+// exponentials.  The only serial hand-off between the groups is the running
+// maximum of each row (and, at the end of a unit, the row sums), passed
+// through shared memory.
 //
 // TMEM per CTA (512 columns allocated):
-//     [0,256)   O half, fp32          [256,320) S, fp32
-//     [320,352) P, bf16 pairs         [352,496) Q half, bf16 pairs
-// Q and P are UMMA A operands read from TMEM; the page tile in shared memory
-// is the B operand of both products: K-major for S (features contiguous),
+//     [0,256)   O half, fp32          [256,320) S, 2 x 32 fp32 columns
+//     [320,352) P, 2 x 16 bf16 pairs  [352,496) Q half, bf16 pairs
+// Q and P are UMMA A operands read from TMEM; the page in shared memory is
+// the B operand of both products: K-major for S (features contiguous),
 // MN-major for O (the same bytes, read along the feature axis).
 //
-// Warp roles (192 threads): warp 0 loads pages with TMA (and zeroes the rows
-// past the end of a partial last page), warp 1 issues UMMA and owns TMEM,
-// warps 2..5 run the softmax, the score exchange and the epilogue with one
-// thread per head row.
+// Warp roles (320 threads):
+//   warp 0      TMA producer: pages into a 4-stage ring (and zeroes the rows
+//               past the end of a partial last page),
+//   warp 1      UMMA issuer (an elected lane of the converged warp) and TMEM
+//               owner: issues each tile's S = Q.K^T as soon as its page and
+//               S buffer are ready and each tile's O += P.C as soon as its P
+//               is, in any order,
+//   warps 2..5  tiles 0, 2, 4, ...: partial S -> peer, peer's partial ->
+//               online softmax -> P into TMEM, lazy rescaling of O, the
+//               query of a unit that starts on their tile, the epilogue of
+//               a unit that ends on it,
+//   warps 6..9  the same for tiles 1, 3, 5, ...
+// Each group covers the four TMEM lane quarters: thread (warp % 4) * 32 +
+// lane owns head row h of the tile.
 //
 // Work split: the pages of all (sequence, token, head-group) units are laid
 // end to end and cut into equal contiguous ranges, one per cluster, so long
@@ -51,33 +70,36 @@
 namespace mla {
 namespace dec {
 
-constexpr int PAGE = 64;       // tokens per page
+constexpr int PAGE = 64;       // tokens per page (TMA unit)
+constexpr int TILE = 32;       // tokens per score tile
 constexpr int DC = 512;        // latent width
 constexpr int DR = 64;         // RoPE key width
 constexpr int HALF_C = 256;    // latent columns per CTA
 constexpr int HALF_R = 32;     // RoPE columns per CTA
 constexpr int HEADS = 128;     // heads per unit (UMMA M)
 constexpr int NSTAGE = 4;      // page pipeline depth
-constexpr int THREADS = 192;
-constexpr int SM_WARP0 = 2;    // first softmax warp
+constexpr int THREADS = 320;
+constexpr int WG_WARP0 = 2;    // warps 2..5: tiles with even index, 6..9: odd
 
 constexpr uint32_t BOX_C_BYTES = PAGE * 128;                      // 64 rows x 64 bf16
 constexpr uint32_t BOX_R_BYTES = PAGE * 64;                       // 64 rows x 32 bf16
 constexpr uint32_t STAGE_BYTES = 4 * BOX_C_BYTES + BOX_R_BYTES;   // 36864
-constexpr uint32_t X_BYTES = HEADS * PAGE * 4;                    // partial S, fp32
+constexpr uint32_t XT_BYTES = HEADS * TILE * 4;                   // one partial S tile, fp32
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_X + 2 * X_BYTES;
-constexpr uint32_t NUM_BARS = 2 * NSTAGE + 11;
-constexpr uint32_t OFF_MISC = OFF_BAR + 8 * 32;
-constexpr uint32_t OFF_SCAN = OFF_MISC + 64;
+constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [2]
+constexpr uint32_t OFF_PUB = OFF_X + 2 * XT_BYTES;  // per-row state handed between the groups
+constexpr uint32_t PUB_BYTES = 2 * 3 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part][128]
+constexpr uint32_t OFF_BAR = OFF_PUB + PUB_BYTES;
+constexpr uint32_t NUM_BARS = 28;
+constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
+constexpr uint32_t OFF_SCAN = OFF_MISC + 128;
 constexpr uint32_t SMEM_BYTES = OFF_SCAN + 8 * THREADS;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1 KB alignment
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, TM_COLS = 512;
 
-// S = Q . K^T: M = 128 heads, N = 64 tokens, both operands K-major.
-constexpr uint32_t IDESC_QK = idesc_bf16(128, 64, false, false);
+// S = Q . K^T: M = 128 heads, N = 32 tokens, both operands K-major.
+constexpr uint32_t IDESC_QK = idesc_bf16(128, TILE, false, false);
 // O += P . C: M = 128 heads, N = 256 latent columns, B MN-major.
 constexpr uint32_t IDESC_PV = idesc_bf16(128, 256, false, true);
 
@@ -226,6 +248,74 @@ inline Walker host_walker(const PlanView& v, int64_t launched, int64_t g) {
     return w;
 }
 
+// Visible tokens of page lp of a segment's unit.
+__device__ __forceinline__ int page_valid(const Segment& sg, int64_t lp) {
+    const int64_t v = sg.un.len - lp * PAGE;
+    return v < PAGE ? (int)v : PAGE;
+}
+
+// Walks the tiles of a cluster's segments in order: pages of 64 tokens, each
+// one or two tiles of 32 (a last page with at most 32 visible tokens has one).
+// Every role of the kernel runs its own copy, so all agree on the sequence
+// and on the global page / tile counters that select ring stages, buffers
+// and barrier phases.
+struct TileIter {
+    Walker w;
+    Segment sg;
+    bool have;
+    int64_t seg, lp, page, tile;  // segment, page within the unit, global page and tile counters
+    int t, ntp, pvalid;           // tile within the page, tiles in it, visible tokens in it
+
+    __device__ void load_page() {
+        pvalid = page_valid(sg, lp);
+        ntp = pvalid > TILE ? 2 : 1;
+        t = 0;
+        ++page;
+    }
+    __device__ void begin(const Walker& w0) {
+        w = w0;
+        seg = -1;
+        page = -1;
+        tile = 0;
+        have = w.next(sg);
+        if (have) {
+            seg = 0;
+            lp = sg.lp0;
+            load_page();
+        }
+    }
+    __device__ void advance() {
+        ++tile;
+        if (t + 1 < ntp) {
+            ++t;
+            return;
+        }
+        if (lp + 1 < sg.lp1) {
+            ++lp;
+            load_page();
+            return;
+        }
+        have = w.next(sg);
+        if (have) {
+            ++seg;
+            lp = sg.lp0;
+            load_page();
+        }
+    }
+    __device__ int valid() const {
+        const int v = pvalid - t * TILE;
+        return v < TILE ? v : TILE;
+    }
+    __device__ bool first_in_seg() const { return lp == sg.lp0 && t == 0; }
+    __device__ bool last_in_page() const { return t + 1 == ntp; }
+    __device__ bool last_in_seg() const { return last_in_page() && lp + 1 == sg.lp1; }
+    __device__ int stage() const { return (int)(page % NSTAGE); }
+    __device__ uint32_t page_parity() const { return (uint32_t)((page / NSTAGE) & 1); }
+    __device__ int buf() const { return (int)(tile & 1); }
+    // parity of this tile's phase of a double-buffered barrier (n tiles back)
+    __device__ uint32_t parity(int back = 0) const { return (uint32_t)(((tile - back) >> 1) & 1); }
+};
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_r,
                    const __grid_constant__ Params p) {
@@ -237,17 +327,21 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
-    auto FULL = [&](int s) { return bar0 + 8u * s; };
-    auto EMPTY = [&](int s) { return bar0 + 8u * (NSTAGE + s); };
-    const uint32_t S_FULL = bar0 + 8u * (2 * NSTAGE + 0);
-    const uint32_t S_FREE = bar0 + 8u * (2 * NSTAGE + 1);
-    const uint32_t P_FULL = bar0 + 8u * (2 * NSTAGE + 2);
-    const uint32_t PV_DONE = bar0 + 8u * (2 * NSTAGE + 3);
-    const uint32_t Q_FULL = bar0 + 8u * (2 * NSTAGE + 4);
-    auto XFULL = [&](int b) { return bar0 + 8u * (2 * NSTAGE + 5 + b); };
-    auto XFREE = [&](int b) { return bar0 + 8u * (2 * NSTAGE + 7 + b); };
-    const uint32_t TAIL = bar0 + 8u * (2 * NSTAGE + 9);
-    const uint32_t DRAIN = bar0 + 8u * (2 * NSTAGE + 10);
+    auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+    auto FULL = [&](int s) { return BAR(s); };
+    auto EMPTY = [&](int s) { return BAR(NSTAGE + s); };
+    auto S_FULL = [&](int b) { return BAR(8 + b); };    // S partial in TMEM (commit)
+    auto S_FREE = [&](int b) { return BAR(10 + b); };   // read by its group (4 warps)
+    auto XFULL = [&](int b) { return BAR(12 + b); };    // peer partial in X (1 arrive + bytes)
+    auto XFREE = [&](int b) { return BAR(14 + b); };    // peer read our copy (4 peer warps)
+    auto P_FULL = [&](int b) { return BAR(16 + b); };   // P in TMEM (4 warps)
+    auto PV_DONE = [&](int b) { return BAR(18 + b); };  // O += P.C of that tile (commit)
+    auto M_PUB = [&](int b) { return BAR(20 + b); };    // running max after the tile (4 warps)
+    auto L_PUB = [&](int b) { return BAR(22 + b); };    // group's row sums after the tile (4 warps)
+    const uint32_t Q_FULL = BAR(24);                    // query of a unit in TMEM (4 warps)
+    const uint32_t O_FREE = BAR(25);                    // epilogue read O (4 warps)
+    const uint32_t TAIL = BAR(26);                      // partial last page landed (TMA)
+    const uint32_t DRAIN = BAR(27);                     // abort: issued MMAs finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + OFF_MISC + 8);
     int64_t* scan = reinterpret_cast<int64_t*>(smem + OFF_SCAN);
@@ -257,15 +351,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             mbar_init(FULL(s), 1);
             mbar_init(EMPTY(s), 1);
         }
-        mbar_init(S_FULL, 1);
-        mbar_init(S_FREE, HEADS);
-        mbar_init(P_FULL, HEADS);
-        mbar_init(PV_DONE, 1);
-        mbar_init(Q_FULL, HEADS);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(S_FULL(b), 1);
+            mbar_init(S_FREE(b), 4);
             mbar_init(XFULL(b), 1);
-            mbar_init(XFREE(b), 4);  // one arrival per softmax warp of the peer
+            mbar_init(XFREE(b), 4);
+            mbar_init(P_FULL(b), 4);
+            mbar_init(PV_DONE(b), 1);
+            mbar_init(M_PUB(b), 4);
+            mbar_init(L_PUB(b), 4);
         }
+        mbar_init(Q_FULL, 4);
+        mbar_init(O_FREE, 4);
         mbar_init(TAIL, 1);
         mbar_init(DRAIN, 1);
         fence_mbar_init_cluster();
@@ -330,12 +427,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             }
         }
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    cluster_sync();  // the peer's barriers are initialised before any remote access
-
-    const uint32_t tmem = *tmem_slot;
+    __syncthreads();  // misc[1], misc[2] (the range's first unit) are written above
     Walker walk;
     walk.v = pv;
     walk.U = U;
@@ -347,6 +439,28 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     walk.u = misc[1];
     walk.pos = misc[2];
     const bool skip = misc[3] != 0;
+    if (threadIdx.x == 0) {
+        // Tiles of this cluster: two per page, less one for each unit piece
+        // whose last page has at most TILE visible tokens.
+        Walker w = walk;
+        Segment sg;
+        int64_t n = 0;
+        while (!skip && w.next(sg)) n += 2 * (sg.lp1 - sg.lp0) - (page_valid(sg, sg.lp1 - 1) > TILE ? 0 : 1);
+        // The peer's partial tiles 0 and 1 will land in X[0], X[1]; later
+        // tiles are armed by the softmax warps as they consume these.
+        for (int64_t i = 0; i < n && i < 2; ++i) mbar_arrive_expect_tx(XFULL((int)i), XT_BYTES);
+        misc[6] = n;
+        for (int g = 0; g < 2; ++g) {
+            misc[7 + g] = n > g ? g + 1 : 0;  // group g: 1 + last tile whose arrival was armed
+            misc[9 + g] = 0;                  // ... and 1 + last tile it consumed
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    cluster_sync();  // the peer's barriers are initialised (and armed) before any remote access
+    const uint32_t tmem = *tmem_slot;
+    const int64_t n_tiles = misc[6];
 
     if (warp == 0) {
         // ========================================================= producer
@@ -367,7 +481,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     pg = 0;
                 }
                 const int y = (int)(pg * PAGE);
-                const int valid = (int)(sg.un.len - lp * PAGE < PAGE ? sg.un.len - lp * PAGE : PAGE);
+                const int valid = page_valid(sg, lp);
                 const uint32_t st = smem_u32(smem + OFF_STAGE + s * STAGE_BYTES);
                 const uint32_t bar = valid == PAGE ? FULL(s) : TAIL;
                 if (lane == 0) {
@@ -417,91 +531,135 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         }
     } else if (warp == 1) {
         // ============================================================== MMA
-        if (lane == 0) {
-            int64_t it = 0, n_qk = 0, n_pv = 0, n_unit = 0;
-            bool ok = !skip;
-            bool issued = false;
-            Segment sg;
-            auto issue_pv = [&](int s, bool first) {
-                const uint32_t st = smem_u32(smem + OFF_STAGE + s * STAGE_BYTES);
-#pragma unroll
-                for (int k = 0; k < PAGE / 16; ++k) {
-                    // C as MN-major B: 64-column boxes 8 KB apart, 8-row
-                    // groups 1 KB apart, 16 tokens = 2 KB per step.
-                    const uint64_t db = smem_desc(st + k * 2048, BOX_C_BYTES, 1024, SWZ_128B);
-                    mma_ts(tmem + TM_O, tmem + TM_P + 8 * k, db, IDESC_PV,
-                           (first && k == 0) ? 0u : 1u);
-                }
-            };
-            while (ok && walk.next(sg)) {
-                ok = mbar_wait(Q_FULL, (uint32_t)(n_unit & 1), 0x301);
-                ++n_unit;
-                if (!ok) break;
-                tc_fence_after();
-                int prev_s = -1;
-                for (int64_t lp = sg.lp0; lp < sg.lp1; ++lp, ++it) {
-                    const int s = (int)(it % NSTAGE);
-                    ok = mbar_wait(FULL(s), (uint32_t)((it / NSTAGE) & 1), 0x302);
-                    if (ok && n_qk > 0) ok = mbar_wait(S_FREE, (uint32_t)((n_qk - 1) & 1), 0x303);
-                    if (!ok) break;
+        // The whole warp polls two queues -- S = Q.K^T of the next tile
+        // (page landed, S buffer drained, query loaded) and O += P.C of the
+        // oldest tile whose P is ready -- and one elected lane issues
+        // whatever is ready, so that the score products run ahead of the
+        // softmax.  Control flow is warp-uniform (readiness is lane 0's view).
+        TileIter qk, pvi;
+        qk.begin(walk);
+        pvi.begin(walk);
+        bool ok = !skip;
+        bool issued = false;
+        uint64_t t_wait = 0;
+        bool waiting = false;
+        const uint64_t dq0 = smem_desc(smem_u32(smem + OFF_STAGE), 16, 1024, SWZ_128B);
+        const uint64_t dr0 = smem_desc(smem_u32(smem + OFF_STAGE + 4 * BOX_C_BYTES), 16, 512, SWZ_64B);
+        const uint64_t dp0 = smem_desc(smem_u32(smem + OFF_STAGE), BOX_C_BYTES, 1024, SWZ_128B);
+        while (ok && pvi.have) {
+            bool progress = false;
+            if (!qk.have || pvi.tile < qk.tile) {
+                const int b = pvi.buf();
+                bool ready = mbar_test(P_FULL(b), pvi.parity());
+                if (ready && pvi.first_in_seg() && pvi.seg > 0)
+                    ready = mbar_test(O_FREE, (uint32_t)((pvi.seg - 1) & 1));
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
                     tc_fence_after();
-                    const uint32_t st = smem_u32(smem + OFF_STAGE + s * STAGE_BYTES);
+                    if (elect_one_sync()) {
+                        // C as MN-major B: 64-column boxes 8 KB apart, 8-row
+                        // groups 1 KB apart, 16 tokens = 2 KB per step.
+                        const uint64_t db = dp0 + ((uint64_t)(pvi.stage() * STAGE_BYTES + pvi.t * (TILE * 128)) >> 4);
+                        const uint32_t acc0 = pvi.first_in_seg() ? 0u : 1u;
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {  // latent features, K-major SW128
-                        const uint64_t db =
-                            smem_desc(st + (k / 4) * BOX_C_BYTES + (k % 4) * 32, 16, 1024, SWZ_128B);
-                        mma_ts(tmem + TM_S, tmem + TM_Q + 8 * k, db, IDESC_QK, k > 0 ? 1u : 0u);
+                        for (int k = 0; k < TILE / 16; ++k)
+                            mma_ts(tmem + TM_O, tmem + TM_P + 16 * b + 8 * k, db + (uint64_t)(k * 2048 >> 4),
+                                   IDESC_PV, k == 0 ? acc0 : 1u);
+                        tc_commit(PV_DONE(b));
+                        if (pvi.last_in_page()) tc_commit(EMPTY(pvi.stage()));
                     }
-#pragma unroll
-                    for (int k = 0; k < 2; ++k) {  // RoPE features, K-major SW64
-                        const uint64_t db = smem_desc(st + 4 * BOX_C_BYTES + k * 32, 16, 512, SWZ_64B);
-                        mma_ts(tmem + TM_S, tmem + TM_Q + 128 + 8 * k, db, IDESC_QK, 1u);
-                    }
-                    issued = true;
-                    tc_commit(S_FULL);
-                    ++n_qk;
-                    if (prev_s >= 0) {
-                        ok = mbar_wait(P_FULL, (uint32_t)(n_pv & 1), 0x304);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_pv(prev_s, lp - 1 == sg.lp0);
-                        tc_commit(PV_DONE);
-                        tc_commit(EMPTY(prev_s));
-                        ++n_pv;
-                    }
-                    prev_s = s;
+                    __syncwarp();
+                    pvi.advance();
+                    progress = true;
                 }
-                if (!ok) break;
-                ok = mbar_wait(P_FULL, (uint32_t)(n_pv & 1), 0x305);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(prev_s, sg.lp1 - 1 == sg.lp0);
-                tc_commit(PV_DONE);
-                tc_commit(EMPTY(prev_s));
-                ++n_pv;
             }
-            if (!ok && issued) {  // wait for the tensor core before TMEM goes away
-                tc_commit(DRAIN);
-                mbar_wait(DRAIN, 0, 0x306);
+            if (qk.have) {
+                const int b = qk.buf();
+                bool ready = qk.t != 0 || mbar_test(FULL(qk.stage()), qk.page_parity());
+                if (ready && qk.tile >= 2) ready = mbar_test(S_FREE(b), qk.parity(2));
+                if (ready && qk.first_in_seg()) ready = mbar_test(Q_FULL, (uint32_t)(qk.seg & 1));
+                if (__shfl_sync(0xffffffffu, ready, 0)) {
+                    tc_fence_after();
+                    if (elect_one_sync()) {
+                        const uint32_t off = (uint32_t)(qk.stage() * STAGE_BYTES);
+                        const uint64_t dc = dq0 + ((uint64_t)(off + qk.t * (TILE * 128)) >> 4);
+                        const uint64_t dr = dr0 + ((uint64_t)(off + qk.t * (TILE * 64)) >> 4);
+                        const uint32_t d = tmem + TM_S + 32 * b;
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)  // latent features, K-major SW128
+                            mma_ts(d, tmem + TM_Q + 8 * k,
+                                   dc + (uint64_t)(((k / 4) * BOX_C_BYTES + (k % 4) * 32) >> 4), IDESC_QK,
+                                   k > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int k = 0; k < 2; ++k)  // RoPE features, K-major SW64
+                            mma_ts(d, tmem + TM_Q + 128 + 8 * k, dr + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
+                        tc_commit(S_FULL(b));
+                    }
+                    __syncwarp();
+                    issued = true;
+                    qk.advance();
+                    progress = true;
+                }
             }
+            if (progress) {
+                waiting = false;
+            } else if (!waiting) {
+                waiting = true;
+                t_wait = global_timer_ns();
+            } else {
+                bool give_up = device_status_raised();
+                if (!give_up && global_timer_ns() - t_wait > MLA_WAIT_LIMIT_NS) {
+                    if (lane == 0) raise_device_status(MLA_DEV_TIMEOUT, 0x301u | ((blockIdx.x & 0xFFFu) << 12));
+                    give_up = true;
+                }
+                ok = !__shfl_sync(0xffffffffu, give_up, 0);
+            }
+        }
+        if (!ok && issued) {  // wait for the tensor core before TMEM goes away
+            if (elect_one_sync()) tc_commit(DRAIN);
+            __syncwarp();
+            mbar_wait_teardown(DRAIN, 0, MLA_WAIT_LIMIT_NS);
         }
         __syncwarp();
     } else {
-        // ==================================================== softmax warps
-        const int q4 = warp & 3;             // TMEM lane quarter of this warp
-        const int h = q4 * 32 + lane;        // head row within the group
+        // ===================================================== tile groups
+        const int grp = (warp - WG_WARP0) / 4;  // tiles with index % 2 == grp
+        const int b = grp;                      // their S, P, X buffers and barriers
+        const int q4 = warp & 3;
+        const int h = q4 * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        const uint32_t x_base = smem_u32(smem + OFF_X);
-        const uint32_t peer_x = map_to_rank(x_base, peer);
-        int64_t n_s = 0, n_pv = 0, n_x = 0;
+        const uint32_t peer_x = map_to_rank(smem_u32(smem + OFF_X + b * XT_BYTES), peer);
+        const uint32_t peer_xfull = map_to_rank(XFULL(b), peer);
+        float* pub = reinterpret_cast<float*>(smem + OFF_PUB);  // [2][3][HEADS]
+        const bool leader = warp == WG_WARP0 + 4 * grp && lane == 0;
+        TileIter it;
+        it.begin(walk);
         bool ok = !skip;
-        Segment sg;
-        while (ok && walk.next(sg)) {
-            const int head = sg.un.hg * HEADS + h;
-            const bool live = head < p.H;
-            const int64_t qrow = ((int64_t)sg.un.b * p.T + sg.un.t) * p.H + head;
-            // ---- this CTA's half of the query row -> TMEM (bf16 pairs)
-            {
+        float m_ref = -INFINITY, l_part = 0.f;  // this group's row sum, relative to m_ref
+        int64_t my_seg = -1;
+        int64_t armed = misc[7 + grp], consumed = 0;
+        while (ok && it.have) {
+            if ((it.tile & 1) != grp) {
+                it.advance();
+                continue;
+            }
+            const int64_t i = it.tile;
+            const bool first = it.first_in_seg();
+            if (my_seg != it.seg) {  // a new unit piece: this group's sums restart
+                my_seg = it.seg;
+                m_ref = -INFINITY;
+                l_part = 0.f;
+            }
+            if (first) {
+                // The query of this unit replaces the last one once every
+                // score product of the tile before has completed.
+                if (i >= 1) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(S_FULL(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x501));
+                    if (!ok) break;
+                }
+                const Unit& un = it.sg.un;
+                const int head = un.hg * HEADS + h;
+                const bool live = head < p.H;
+                const int64_t qrow = ((int64_t)un.b * p.T + un.t) * p.H + head;
                 const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat + qrow * DC + rank * HALF_C);
                 const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * DR + rank * HALF_R);
 #pragma unroll
@@ -529,152 +687,199 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 tmem_st16(trow + TM_Q + 128, r);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(Q_FULL);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(Q_FULL);
             }
-            float m_used = -INFINITY, l = 0.f;
-            for (int64_t lp = sg.lp0; lp < sg.lp1; ++lp) {
-                // ---- partial scores of this CTA's features
-                ok = __all_sync(0xffffffffu, mbar_wait(S_FULL, (uint32_t)(n_s & 1), 0x401));
-                ++n_s;
+            // ---- own partial scores: TMEM -> registers -> the peer
+            ok = __all_sync(0xffffffffu, mbar_wait(S_FULL(b), it.parity(), 0x502));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t own[TILE];
+            tmem_ld32(trow + TM_S + 32 * b, own);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S_FREE(b));
+            if (i >= 2) {  // the peer has read our copy of the tile two back
+                ok = __all_sync(0xffffffffu, mbar_wait(XFREE(b), it.parity(2), 0x503));
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int k = 0; k < TILE / 4; ++k)
+                st_async_v4(peer_x + (uint32_t)(k * HEADS + h) * 16u, own[4 * k], own[4 * k + 1], own[4 * k + 2],
+                            own[4 * k + 3], peer_xfull);
+            // ---- plus the peer's partial, from X[b]
+            ok = __all_sync(0xffffffffu, mbar_wait<true>(XFULL(b), it.parity(), 0x504));
+            if (!ok) break;
+            consumed = i + 1;
+            if (leader && i + 2 < n_tiles) {
+                mbar_arrive_expect_tx(XFULL(b), XT_BYTES);  // X[b] next receives tile i + 2
+                armed = i + 3;
+            }
+            const float4* xp = reinterpret_cast<const float4*>(smem + OFF_X + b * XT_BYTES);
+            const int valid = it.valid();
+            float s[TILE];
+#pragma unroll
+            for (int k = 0; k < TILE / 4; ++k) {
+                const float4 c = xp[k * HEADS + h];
+                s[4 * k] = (__uint_as_float(own[4 * k]) + c.x) * p.scale_log2;
+                s[4 * k + 1] = (__uint_as_float(own[4 * k + 1]) + c.y) * p.scale_log2;
+                s[4 * k + 2] = (__uint_as_float(own[4 * k + 2]) + c.z) * p.scale_log2;
+                s[4 * k + 3] = (__uint_as_float(own[4 * k + 3]) + c.w) * p.scale_log2;
+            }
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int j = 0; j < TILE; ++j) {
+                if (j >= valid) s[j] = -INFINITY;
+                mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
+            }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            // ---- the running maximum after the tile before (the other group)
+            float m_prev = -INFINITY;
+            if (i >= 1) {
+                ok = __all_sync(0xffffffffu, mbar_wait(M_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x505));
+                if (!ok) break;
+                m_prev = pub[(b ^ 1) * 3 * HEADS + h];
+            }
+            const bool last = it.last_in_seg();
+            float m_oth = -INFINITY, l_oth = 0.f;  // the other group's sums (unit's last tile only)
+            if (last && !first) {
+                // before this tile's maximum is published, so that the other
+                // group cannot publish its next tile's sums over these
+                ok = __all_sync(0xffffffffu, mbar_wait(L_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x506));
+                if (!ok) break;
+                m_oth = pub[((b ^ 1) * 3 + 1) * HEADS + h];
+                l_oth = pub[((b ^ 1) * 3 + 2) * HEADS + h];
+            }
+            float m_used;
+            bool need = false;
+            if (first) {
+                m_used = mx;
+            } else {
+                need = mx > m_prev + RESCALE_THRESHOLD;
+                m_used = need ? mx : m_prev;
+            }
+            if (__any_sync(0xffffffffu, need)) {
+                // O moves to the new maximum once the tile before has been
+                // added to it, and before any later tile is
+                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x507));
                 if (!ok) break;
                 tc_fence_after();
-                float s[PAGE];
-                {
+                const float alpha = ex2(m_prev - m_used);
+#pragma unroll 1
+                for (int c = 0; c < HALF_C; c += 32) {
                     uint32_t r[32];
-                    tmem_ld32(trow + TM_S, r);
+                    tmem_ld32(trow + TM_O + c, r);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(r[j]);
-                    tmem_ld32(trow + TM_S + 32, r);
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(r[j]);
+                    for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+                    tmem_st32(trow + TM_O + c, r);
                 }
+                tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(S_FREE);
-                // ---- exchange with the peer: send ours, receive theirs
-                const int xb = (int)(n_x & 1);
-                const uint32_t xph = (uint32_t)((n_x >> 1) & 1);
-                ++n_x;
-                ok = __all_sync(0xffffffffu, mbar_wait<true>(XFREE(xb), xph ^ 1u, 0x402));
+            }
+            pub[b * 3 * HEADS + h] = m_used;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(M_PUB(b));
+            if (m_ref != m_used) {  // this group's earlier sums, to the new reference
+                l_part = m_ref == -INFINITY ? 0.f : l_part * ex2(m_ref - m_used);
+                m_ref = m_used;
+            }
+            // ---- P[b] is free once the tile two back has been multiplied
+            if (i >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b), it.parity(2), 0x508));
                 if (!ok) break;
-                {
-                    const uint32_t dst = peer_x + xb * X_BYTES;
-                    const uint32_t pbar = map_to_rank(XFULL(xb), peer);
+                tc_fence_after();
+            }
+            {
+                uint32_t pk[TILE / 2];
+                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        st_async_v4(dst + (k * HEADS + h) * 16, __float_as_uint(s[4 * k]),
-                                    __float_as_uint(s[4 * k + 1]), __float_as_uint(s[4 * k + 2]),
-                                    __float_as_uint(s[4 * k + 3]), pbar);
+                for (int j = 0; j < TILE / 2; ++j) {
+                    const float p0 = ex2(s[2 * j] - m_used);
+                    const float p1 = ex2(s[2 * j + 1] - m_used);
+                    sum4[j & 3] += p0 + p1;
+                    pk[j] = pack_bf16x2(p0, p1);
                 }
-                if (h == 0) mbar_arrive_expect_tx(XFULL(xb), X_BYTES);
-                ok = __all_sync(0xffffffffu, mbar_wait<true>(XFULL(xb), xph, 0x403));
+                l_part += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                tmem_st16(trow + TM_P + 16 * b, pk);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            pub[(b * 3 + 1) * HEADS + h] = m_ref;
+            pub[(b * 3 + 2) * HEADS + h] = l_part;
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(P_FULL(b));
+                mbar_arrive(L_PUB(b));
+                // Every value read from X[b] has gone into P, now stored.
+                mbar_arrive_remote_relaxed(map_to_rank(XFREE(b), peer));
+            }
+            if (last) {
+                // ---- epilogue: O / l of this CTA's 256 columns, lse
+                const Segment& sg = it.sg;
+                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b), it.parity(), 0x509));
                 if (!ok) break;
-                {
-                    const float4* src = reinterpret_cast<const float4*>(smem + OFF_X + xb * X_BYTES);
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const float4 v = src[k * HEADS + h];
-                        s[4 * k] += v.x;
-                        s[4 * k + 1] += v.y;
-                        s[4 * k + 2] += v.z;
-                        s[4 * k + 3] += v.w;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(map_to_rank(XFREE(xb), peer));
-                // ---- online softmax (base 2), lazily rescaled
-                const int valid = (int)(sg.un.len - lp * PAGE < PAGE ? sg.un.len - lp * PAGE : PAGE);
-                float mx = -INFINITY;
-#pragma unroll
-                for (int j = 0; j < PAGE; ++j) {
-                    s[j] = j < valid ? s[j] * p.scale_log2 : -INFINITY;
-                    mx = fmaxf(mx, s[j]);
-                }
-                const bool first = lp == sg.lp0;
-                if (first) m_used = mx;
-                const bool need = !first && mx > m_used + RESCALE_THRESHOLD;
-                if (!first) {  // PV of the previous page done: P is free, O is stable
-                    ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE, (uint32_t)(n_pv & 1), 0x404));
-                    ++n_pv;
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                if (__any_sync(0xffffffffu, need)) {
-                    const float m_new = need ? mx : m_used;
-                    const float alpha = ex2(m_used - m_new);
+                tc_fence_after();
+                const float l = l_part + (first ? 0.f : l_oth * ex2(m_oth - m_used));
+                const int head = sg.un.hg * HEADS + h;
+                const bool live = head < p.H;
+                const int64_t qrow = ((int64_t)sg.un.b * p.T + sg.un.t) * p.H + head;
+                const float inv_l = 1.f / l;
+                if (sg.slot < 0) {
+                    __nv_bfloat16* dst = p.o + qrow * DC + rank * HALF_C;
 #pragma unroll 1
                     for (int c = 0; c < HALF_C; c += 32) {
                         uint32_t r[32];
                         tmem_ld32(trow + TM_O + c, r);
+                        if (live) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                        tmem_st32(trow + TM_O + c, r);
+                            for (int v = 0; v < 4; ++v)
+                                d4[v] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(r[8 * v]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l),
+                                    pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l));
+                        }
                     }
-                    l *= alpha;
-                    m_used = m_new;
-                }
-                {
-                    uint32_t pk[32];
-                    float sum = 0.f;
+                    if (live && rank == 0) p.lse[qrow] = (m_used + __log2f(l)) * LN2;
+                } else {
+                    float* dst = p.ws_o + (sg.slot * HEADS + h) * DC + rank * HALF_C;
+#pragma unroll 1
+                    for (int c = 0; c < HALF_C; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(trow + TM_O + c, r);
+                        float4* d4 = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float p0 = ex2(s[2 * j] - m_used);
-                        const float p1 = ex2(s[2 * j + 1] - m_used);
-                        sum += p0 + p1;
-                        pk[j] = pack_bf16x2(p0, p1);
+                        for (int v = 0; v < 8; ++v)
+                            d4[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
+                                                __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
                     }
-                    l += sum;
-                    tmem_st32(trow + TM_P, pk);
+                    if (rank == 0) p.ws_lse[sg.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
                 }
-                tmem_st_wait();
+                if (rank == 0 && h == 0 && sg.g_first == walk.g)
+                    p.ws_unit[sg.u] = make_int2((int)sg.g_first, (int)sg.g_last);
                 tc_fence_before();
-                mbar_arrive(P_FULL);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(O_FREE);
             }
-            if (!ok) break;
-            // ---- epilogue: O / l of this CTA's 256 columns, lse
-            ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE, (uint32_t)(n_pv & 1), 0x405));
-            ++n_pv;
-            if (!ok) break;
-            tc_fence_after();
-            const float inv_l = 1.f / l;
-            if (sg.slot < 0) {
-                __nv_bfloat16* dst = p.o + qrow * DC + rank * HALF_C;
-#pragma unroll 1
-                for (int c = 0; c < HALF_C; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(trow + TM_O + c, r);
-                    if (live) {
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            d4[v] = make_uint4(
-                                pack_bf16x2(__uint_as_float(r[8 * v]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l),
-                                pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l));
-                    }
-                }
-                if (live && rank == 0) p.lse[qrow] = (m_used + __log2f(l)) * LN2;
-            } else {
-                float* dst = p.ws_o + (sg.slot * HEADS + h) * DC + rank * HALF_C;
-#pragma unroll 1
-                for (int c = 0; c < HALF_C; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(trow + TM_O + c, r);
-                    float4* d4 = reinterpret_cast<float4*>(dst + c);
-#pragma unroll
-                    for (int v = 0; v < 8; ++v)
-                        d4[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                            __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
-                }
-                if (rank == 0) p.ws_lse[sg.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
-            }
-            if (rank == 0 && h == 0 && sg.g_first == walk.g)
-                p.ws_unit[sg.u] = make_int2((int)sg.g_first, (int)sg.g_last);
+            it.advance();
+        }
+        if (leader) {
+            misc[7 + grp] = armed;
+            misc[9 + grp] = consumed;
         }
     }
 
     tc_fence_before();
     __syncthreads();
+    // Teardown: a partial S tile the peer may still be copying into X lands
+    // before this CTA's shared memory can go away (only after an abort can
+    // one be armed but not consumed; the wait gives up after 10 ms).
+    if (threadIdx.x == 0) {
+        for (int g = 0; g < 2; ++g)
+            if (misc[7 + g] > misc[9 + g])
+                mbar_wait_teardown(XFULL(g), (uint32_t)(((misc[7 + g] - 1) >> 1) & 1), 10000000ull);
+    }
     if (warp == 1) tmem_dealloc(tmem, TM_COLS);
     cluster_sync();
 }

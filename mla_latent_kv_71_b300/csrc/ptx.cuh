@@ -27,7 +27,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
     return t;
 }
 
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
+// One lane of a converged warp (elect.sync).  tcgen05.mma issues at the
+// tensor core's rate only from an elected lane of a converged warp; issued
+// from a lone lane of a diverged warp each instruction costs several times
+// more (measured on B300).
+__device__ __forceinline__ bool elect_one_sync() {
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
 
 // ---------------------------------------------------------------- mbarrier
 
@@ -80,6 +92,19 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
     return ok != 0;
 }
 
+// Non-blocking probe: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  `where` is recorded in
 // the status word's detail field when the wait gives up.
 template <bool kCluster = false>
@@ -95,6 +120,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
             return false;
         }
     }
+}
+
+// Wait with its own time limit that ignores the device status word (used on
+// teardown paths, to let copies already in flight land before the CTA exits).
+__device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait_cluster(bar, parity))
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    return true;
 }
 
 // --------------------------------------------------------------------- TMA
@@ -182,6 +216,27 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
         "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
             "r"(remote_addr),
         "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+        : "memory");
+}
+
+// Arrive on a barrier of another CTA of the cluster without ordering any
+// other memory operation (no cluster-scope fence).  Used only to hand a
+// buffer back after reading it, and issued after every value read from that
+// buffer has been consumed by a completed operation, so the reads are done.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+                 : "memory");
+}
+
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// this CTA's shared memory into another CTA's shared memory; completion is
+// counted as transaction bytes on the destination CTA's barrier.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t dst_bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            dst_cluster),
+        "r"(src_cta), "r"(bytes), "r"(dst_bar_cluster)
         : "memory");
 }
 
