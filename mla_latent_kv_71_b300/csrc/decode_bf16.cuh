@@ -40,15 +40,17 @@
 // Warp roles (320 threads):
 //   warp 0      TMA producer: pages into a 4-stage ring (and zeroes the rows
 //               past the end of a partial last page),
-//   warp 1      UMMA issuer (an elected lane of the converged warp) and TMEM
-//               owner: issues each tile's S = Q.K^T as soon as its page and
-//               S buffer are ready and each tile's O += P.C as soon as its P
-//               is, in any order,
-//   warps 2..5  tiles 0, 2, 4, ...: partial S -> peer, peer's partial ->
-//               online softmax -> P into TMEM, lazy rescaling of O, the
+//   warp 1      TMEM owner; an elected lane issues each tile's S = Q.K^T as
+//               soon as its page has landed and its S buffer has been read,
+//   warp 2      an elected lane issues each tile's O += P.C, in tile order,
+//               as soon as its P is in TMEM,
+//   warps 3..6  tiles 0, 2, 4, ...: partial S -> peer, peer's partial ->
+//               online softmax -> P into TMEM; lazy rescaling of O, the
 //               query of a unit that starts on their tile, the epilogue of
 //               a unit that ends on it,
-//   warps 6..9  the same for tiles 1, 3, 5, ...
+//   warps 7..10 the same for tiles 1, 3, 5, ...
+// The control warps wait with suspended (blocking) mbarrier waits, so they
+// take no issue slots from the tile groups that share their sub-partitions.
 // Each group covers the four TMEM lane quarters: thread (warp % 4) * 32 +
 // lane owns head row h of the tile.
 //
@@ -78,22 +80,21 @@ constexpr int HALF_C = 256;    // latent columns per CTA
 constexpr int HALF_R = 32;     // RoPE columns per CTA
 constexpr int HEADS = 128;     // heads per unit (UMMA M)
 constexpr int NSTAGE = 4;      // page pipeline depth
-constexpr int THREADS = 320;
-constexpr int WG_WARP0 = 2;    // warps 2..5: tiles with even index, 6..9: odd
+constexpr int THREADS = 352;
+constexpr int WG_WARP0 = 3;    // warps 3..6: tiles with even index, 7..10: odd
 
 constexpr uint32_t BOX_C_BYTES = PAGE * 128;                      // 64 rows x 64 bf16
 constexpr uint32_t BOX_R_BYTES = PAGE * 64;                       // 64 rows x 32 bf16
 constexpr uint32_t STAGE_BYTES = 4 * BOX_C_BYTES + BOX_R_BYTES;   // 36864
 constexpr uint32_t XT_BYTES = HEADS * TILE * 4;                   // one partial S tile, fp32
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [2]
-constexpr uint32_t OFF_PUB = OFF_X + 2 * XT_BYTES;  // per-row state handed between the groups
+constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [group][slot]
+constexpr uint32_t OFF_PUB = OFF_X + 4 * XT_BYTES;  // per-row state handed between the groups
 constexpr uint32_t PUB_BYTES = 2 * 3 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part][128]
 constexpr uint32_t OFF_BAR = OFF_PUB + PUB_BYTES;
-constexpr uint32_t NUM_BARS = 28;
+constexpr uint32_t NUM_BARS = 38;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
-constexpr uint32_t OFF_SCAN = OFF_MISC + 128;
-constexpr uint32_t SMEM_BYTES = OFF_SCAN + 8 * THREADS;
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1 KB alignment
 
 constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, TM_COLS = 512;
@@ -143,42 +144,46 @@ struct PlanView {
     int B, T, HG, max_pages, causal;
 };
 
+// Plan quantities (units, pages of the line, clusters, slots, tiles) are
+// 32-bit: the host rejects shapes where B*T*HG*max_pages or max_pages*64
+// reach 2^31, which bounds all of them.
+
 // Visible positions and pages of unit u.
 struct Unit {
     int b, t, hg;
-    int64_t len;    // visible positions
-    int64_t pages;  // ceil(len / 64)
-    bool bad_len;   // seq_lens[b] outside [0, max_pages * 64] (clamped)
+    int len;       // visible positions
+    int pages;     // ceil(len / 64)
+    bool bad_len;  // seq_lens[b] outside [0, max_pages * 64] (clamped)
 };
 
-__host__ __device__ __forceinline__ Unit unit_of(const PlanView& v, int64_t u) {
+__host__ __device__ __forceinline__ Unit unit_of(const PlanView& v, int u) {
     Unit r;
-    const int64_t bt = u / v.HG;
-    r.hg = (int)(u % v.HG);
-    r.b = (int)(bt / v.T);
-    r.t = (int)(bt % v.T);
-    int64_t len = v.seq_lens[r.b];
-    const int64_t cap = (int64_t)v.max_pages * PAGE;
+    const int bt = u / v.HG;
+    r.hg = u % v.HG;
+    r.b = bt / v.T;
+    r.t = bt % v.T;
+    int len = v.seq_lens[r.b];
+    const int cap = v.max_pages * PAGE;
     r.bad_len = len < 0 || len > cap;
     if (r.bad_len) len = len < 0 ? 0 : cap;
-    const int64_t n = v.causal ? len - (v.T - 1 - r.t) : len;
+    const int n = v.causal ? len - (v.T - 1 - r.t) : len;
     r.len = n < 0 ? 0 : n;
     r.pages = (r.len + PAGE - 1) / PAGE;
     return r;
 }
 
-__host__ __device__ __forceinline__ int64_t range_start(int64_t total, int64_t g, int64_t G) {
-    return total * g / G;
+__host__ __device__ __forceinline__ int range_start(int total, int g, int G) {
+    return (int)((int64_t)total * g / G);
 }
 
 // Clusters used for `total` pages when `launched` clusters run.
-__host__ __device__ __forceinline__ int64_t clusters_used(int64_t total, int64_t launched) {
+__host__ __device__ __forceinline__ int clusters_used(int total, int launched) {
     return total < launched ? total : launched;
 }
 
 // The range (cluster) holding page x of the line.
-__host__ __device__ __forceinline__ int64_t cluster_of_page(int64_t x, int64_t total, int64_t G) {
-    int64_t g = x * G / total;
+__host__ __device__ __forceinline__ int cluster_of_page(int x, int total, int G) {
+    int g = (int)((int64_t)x * G / total);
     while (g + 1 < G && range_start(total, g + 1, G) <= x) ++g;
     while (g > 0 && range_start(total, g, G) > x) --g;
     return g;
@@ -186,28 +191,27 @@ __host__ __device__ __forceinline__ int64_t cluster_of_page(int64_t x, int64_t t
 
 // A piece of a unit processed by one cluster.
 struct Segment {
-    int64_t u;
-    Unit un;
-    int64_t lp0, lp1;          // page range within the unit
-    int64_t slot;              // partial slot, or -1 when the whole unit is here
-    int64_t g_first, g_last;   // clusters holding the unit's first and last page
+    int u;
+    int len;               // visible positions of the unit
+    int lp0, lp1;          // page range within the unit
+    int slot;              // partial slot, or -1 when the whole unit is here
+    int g_first, g_last;   // clusters holding the unit's first and last page
 };
 
 // Walks the units overlapping cluster g's range, in line order.
 struct Walker {
-    PlanView v;
-    int64_t U, rs, re, total, G, g;
-    int64_t u, pos;  // next unit and its first page on the line
-    __host__ __device__ bool next(Segment& s) {
+    int U, rs, re, total, G, g;
+    int u, pos;  // next unit and its first page on the line
+    __host__ __device__ bool next(const PlanView& v, Segment& s) {
         if (rs >= re) return false;  // an empty range has no piece
         while (pos < re && u < U) {
             const Unit un = unit_of(v, u);
-            const int64_t start = pos;
+            const int start = pos;
             pos += un.pages;
-            const int64_t cu = u++;
+            const int cu = u++;
             if (un.pages == 0 || pos <= rs) continue;
             s.u = cu;
-            s.un = un;
+            s.len = un.len;
             s.lp0 = (rs > start ? rs : start) - start;
             s.lp1 = (re < pos ? re : pos) - start;
             s.g_first = cluster_of_page(start, total, G);
@@ -220,12 +224,11 @@ struct Walker {
 };
 
 // Walker of cluster g, found by a sequential scan (host side).
-inline Walker host_walker(const PlanView& v, int64_t launched, int64_t g) {
+inline Walker host_walker(const PlanView& v, int launched, int g) {
     Walker w;
-    w.v = v;
-    w.U = (int64_t)v.B * v.T * v.HG;
-    int64_t total = 0;
-    for (int64_t u = 0; u < w.U; ++u) total += unit_of(v, u).pages;
+    w.U = v.B * v.T * v.HG;
+    int total = 0;
+    for (int u = 0; u < w.U; ++u) total += unit_of(v, u).pages;
     w.total = total;
     w.G = clusters_used(total, launched);
     w.g = g;
@@ -235,9 +238,9 @@ inline Walker host_walker(const PlanView& v, int64_t launched, int64_t g) {
     if (total == 0 || g >= w.G) return w;
     w.rs = range_start(total, g, w.G);
     w.re = range_start(total, g + 1, w.G);
-    int64_t pos = 0;
-    for (int64_t u = 0; u < w.U; ++u) {
-        const int64_t n = unit_of(v, u).pages;
+    int pos = 0;
+    for (int u = 0; u < w.U; ++u) {
+        const int n = unit_of(v, u).pages;
         if (w.rs < pos + n) {
             w.u = u;
             w.pos = pos;
@@ -248,10 +251,16 @@ inline Walker host_walker(const PlanView& v, int64_t launched, int64_t g) {
     return w;
 }
 
+// Host-side bound check for the 32-bit plan arithmetic.
+inline bool plan_fits_int32(int B, int T, int HG, int max_pages) {
+    return (int64_t)B * T * HG * max_pages < ((int64_t)1 << 31) &&
+           (int64_t)max_pages * PAGE < ((int64_t)1 << 31);
+}
+
 // Visible tokens of page lp of a segment's unit.
-__device__ __forceinline__ int page_valid(const Segment& sg, int64_t lp) {
-    const int64_t v = sg.un.len - lp * PAGE;
-    return v < PAGE ? (int)v : PAGE;
+__device__ __forceinline__ int page_valid(const Segment& sg, int lp) {
+    const int v = sg.len - lp * PAGE;
+    return v < PAGE ? v : PAGE;
 }
 
 // Walks the tiles of a cluster's segments in order: pages of 64 tokens, each
@@ -263,7 +272,7 @@ struct TileIter {
     Walker w;
     Segment sg;
     bool have;
-    int64_t seg, lp, page, tile;  // segment, page within the unit, global page and tile counters
+    int seg, lp, page, tile;      // segment, page within the unit, global page and tile counters
     int t, ntp, pvalid;           // tile within the page, tiles in it, visible tokens in it
 
     __device__ void load_page() {
@@ -272,19 +281,19 @@ struct TileIter {
         t = 0;
         ++page;
     }
-    __device__ void begin(const Walker& w0) {
+    __device__ void begin(const Walker& w0, const PlanView& v) {
         w = w0;
         seg = -1;
         page = -1;
         tile = 0;
-        have = w.next(sg);
+        have = w.next(v, sg);
         if (have) {
             seg = 0;
             lp = sg.lp0;
             load_page();
         }
     }
-    __device__ void advance() {
+    __device__ void advance(const PlanView& v) {
         ++tile;
         if (t + 1 < ntp) {
             ++t;
@@ -295,7 +304,7 @@ struct TileIter {
             load_page();
             return;
         }
-        have = w.next(sg);
+        have = w.next(v, sg);
         if (have) {
             ++seg;
             lp = sg.lp0;
@@ -316,6 +325,28 @@ struct TileIter {
     __device__ uint32_t parity(int back = 0) const { return (uint32_t)(((tile - back) >> 1) & 1); }
 };
 
+// What a tile group keeps of a tile between its two halves of work.
+struct TileInfo {
+    int tile, seg, u, slot, g_first, g_last, valid, stage, tp;
+    bool first, last, last_in_page;
+    __device__ void set(const TileIter& it) {
+        stage = it.stage();
+        tp = it.t;
+        last_in_page = it.last_in_page();
+        tile = it.tile;
+        seg = it.seg;
+        u = it.sg.u;
+        slot = it.sg.slot;
+        g_first = it.sg.g_first;
+        g_last = it.sg.g_last;
+        valid = it.valid();
+        first = it.first_in_seg();
+        last = it.last_in_seg();
+    }
+};
+
+// 11 warps share 4 register-file quarters (at most 3 warps each), so a
+// thread may use at most 168 registers.
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
 decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_r,
                    const __grid_constant__ Params p) {
@@ -332,19 +363,19 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     auto EMPTY = [&](int s) { return BAR(NSTAGE + s); };
     auto S_FULL = [&](int b) { return BAR(8 + b); };    // S partial in TMEM (commit)
     auto S_FREE = [&](int b) { return BAR(10 + b); };   // read by its group (4 warps)
-    auto XFULL = [&](int b) { return BAR(12 + b); };    // peer partial in X (1 arrive + bytes)
-    auto XFREE = [&](int b) { return BAR(14 + b); };    // peer read our copy (4 peer warps)
-    auto P_FULL = [&](int b) { return BAR(16 + b); };   // P in TMEM (4 warps)
-    auto PV_DONE = [&](int b) { return BAR(18 + b); };  // O += P.C of that tile (commit)
-    auto M_PUB = [&](int b) { return BAR(20 + b); };    // running max after the tile (4 warps)
-    auto L_PUB = [&](int b) { return BAR(22 + b); };    // group's row sums after the tile (4 warps)
-    const uint32_t Q_FULL = BAR(24);                    // query of a unit in TMEM (4 warps)
-    const uint32_t O_FREE = BAR(25);                    // epilogue read O (4 warps)
-    const uint32_t TAIL = BAR(26);                      // partial last page landed (TMA)
-    const uint32_t DRAIN = BAR(27);                     // abort: issued MMAs finished
+    // the peer's partial tile i lands in X[i % 2][(i / 2) % 2]: x = 2 * (i % 2) + (i / 2) % 2
+    auto XFULL = [&](int x) { return BAR(12 + x); };    // peer partial in X (1 arrive + bytes)
+    auto XFREE = [&](int x) { return BAR(16 + x); };    // peer read our copy (4 peer warps)
+    auto PV_DONE = [&](int b) { return BAR(20 + b); };  // O += P.C of that tile (commit)
+    auto M_PUB = [&](int b) { return BAR(22 + b); };    // running max after the tile (4 warps)
+    auto L_PUB = [&](int b) { return BAR(24 + b); };    // group's row sums after the tile (4 warps)
+    const uint32_t Q_FULL = BAR(26);                    // query of a unit in TMEM (4 warps)
+    const uint32_t O_FREE = BAR(27);                    // epilogue read O (4 warps)
+    const uint32_t TAIL = BAR(28);                      // partial last page landed (TMA)
+    auto DRAIN = [&](int k) { return BAR(29 + k); };    // abort: MMAs of warp 1 + k finished
+    auto P_FULL = [&](int b) { return BAR(31 + b); };   // P in TMEM (4 warps)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + OFF_MISC + 8);
-    int64_t* scan = reinterpret_cast<int64_t*>(smem + OFF_SCAN);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -354,17 +385,19 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         for (int b = 0; b < 2; ++b) {
             mbar_init(S_FULL(b), 1);
             mbar_init(S_FREE(b), 4);
-            mbar_init(XFULL(b), 1);
-            mbar_init(XFREE(b), 4);
-            mbar_init(P_FULL(b), 4);
             mbar_init(PV_DONE(b), 1);
+            mbar_init(P_FULL(b), 4);
             mbar_init(M_PUB(b), 4);
             mbar_init(L_PUB(b), 4);
+        }
+        for (int x = 0; x < 4; ++x) {
+            mbar_init(XFULL(x), 1);
+            mbar_init(XFREE(x), 4);
         }
         mbar_init(Q_FULL, 4);
         mbar_init(O_FREE, 4);
         mbar_init(TAIL, 1);
-        mbar_init(DRAIN, 1);
+        for (int k = 0; k < 2; ++k) mbar_init(DRAIN(k), 1);
         fence_mbar_init_cluster();
     }
     if (warp == 0 && lane == 0) {
@@ -384,9 +417,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     pv.causal = p.causal;
     const int64_t U = (int64_t)p.B * p.T * p.HG;
     const int64_t launched = num_clusters_x(), g_id = cluster_id_x();
-    {
-        const int64_t chunk = (U + THREADS - 1) / THREADS;
-        const int64_t u0 = min(U, (int64_t)threadIdx.x * chunk), u1 = min(U, u0 + chunk);
+    if (warp == 0) {
+        // Warp 0 sums the pages of contiguous chunks of units and scans them
+        // with shuffles; the lane holding the range start finds its unit.
+        const int64_t chunk = (U + 31) / 32;
+        const int64_t u0 = min(U, (int64_t)lane * chunk), u1 = min(U, u0 + chunk);
         int64_t sum = 0;
         bool bad = false;
         for (int64_t u = u0; u < u1; ++u) {
@@ -395,25 +430,23 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             bad |= un.bad_len;
         }
         if (bad && rank == 0 && g_id == 0) raise_device_status(MLA_DEV_BOUNDS, 0x10);
-        scan[threadIdx.x] = sum;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int64_t acc = 0;
-            for (int i = 0; i < THREADS; ++i) {
-                const int64_t v = scan[i];
-                scan[i] = acc;
-                acc += v;
-            }
-            misc[0] = acc;  // total pages
-            misc[1] = U;    // first unit of this cluster's range (default: none)
+        int64_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+        const int64_t pre = incl - sum;
+        if (lane == 0) {
+            misc[0] = total;  // total pages
+            misc[1] = U;      // first unit of this cluster's range (default: none)
             misc[2] = 0;
             misc[3] = device_status_raised() ? 1 : 0;  // one decision for the whole CTA
         }
-        __syncthreads();
-        const int64_t total = misc[0];
+        __syncwarp();
         const int64_t G = clusters_used(total, launched);
         const int64_t rs = g_id < G ? range_start(total, g_id, G) : total;
-        const int64_t pre = scan[threadIdx.x];
         if (g_id < G && rs >= pre && rs < pre + sum) {
             int64_t pos = pre;
             for (int64_t u = u0; u < u1; ++u) {
@@ -429,7 +462,6 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     }
     __syncthreads();  // misc[1], misc[2] (the range's first unit) are written above
     Walker walk;
-    walk.v = pv;
     walk.U = U;
     walk.total = misc[0];
     walk.G = clusters_used(walk.total, launched);
@@ -445,14 +477,15 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         Walker w = walk;
         Segment sg;
         int64_t n = 0;
-        while (!skip && w.next(sg)) n += 2 * (sg.lp1 - sg.lp0) - (page_valid(sg, sg.lp1 - 1) > TILE ? 0 : 1);
-        // The peer's partial tiles 0 and 1 will land in X[0], X[1]; later
-        // tiles are armed by the softmax warps as they consume these.
-        for (int64_t i = 0; i < n && i < 2; ++i) mbar_arrive_expect_tx(XFULL((int)i), XT_BYTES);
+        while (!skip && w.next(pv, sg)) n += 2 * (sg.lp1 - sg.lp0) - (page_valid(sg, sg.lp1 - 1) > TILE ? 0 : 1);
+        // The peer's partial tiles 0..3 land in the four X buffers; later
+        // tiles are armed by the groups as they consume these.
+        for (int64_t i = 0; i < n && i < 4; ++i)
+            mbar_arrive_expect_tx(XFULL((int)(2 * (i & 1) + ((i >> 1) & 1))), XT_BYTES);
         misc[6] = n;
         for (int g = 0; g < 2; ++g) {
-            misc[7 + g] = n > g ? g + 1 : 0;  // group g: 1 + last tile whose arrival was armed
-            misc[9 + g] = 0;                  // ... and 1 + last tile it consumed
+            misc[7 + g] = n < 4 ? n : 4;  // group g: tiles below this were armed
+            misc[9 + g] = 0;              // ... and its tiles below this consumed
         }
     }
     tc_fence_before();
@@ -469,13 +502,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         uint32_t tail_phase = 0;
         bool ok = !skip;
         Segment sg;
-        while (ok && walk.next(sg)) {
+        while (ok && walk.next(pv, sg)) {
             for (int64_t lp = sg.lp0; lp < sg.lp1 && ok; ++lp, ++it) {
                 const int s = (int)(it % NSTAGE);
                 ok = mbar_wait(EMPTY(s), (uint32_t)((it / NSTAGE) & 1) ^ 1u, 0x201);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                int64_t pg = p.page_table[(int64_t)sg.un.b * p.max_pages + lp];
+                const int b_seq = sg.u / (p.HG * p.T);  // unit u = (b * T + t) * HG + hg
+                int64_t pg = p.page_table[(int64_t)b_seq * p.max_pages + lp];
                 if (pg < 0 || pg >= p.num_pages) {
                     raise_device_status(MLA_DEV_BOUNDS, 0x20);
                     pg = 0;
@@ -530,136 +564,127 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 mbar_wait(EMPTY((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), 0x204);
         }
     } else if (warp == 1) {
-        // ============================================================== MMA
-        // The whole warp polls two queues -- S = Q.K^T of the next tile
-        // (page landed, S buffer drained, query loaded) and O += P.C of the
-        // oldest tile whose P is ready -- and one elected lane issues
-        // whatever is ready, so that the score products run ahead of the
-        // softmax.  Control flow is warp-uniform (readiness is lane 0's view).
-        TileIter qk, pvi;
-        qk.begin(walk);
-        pvi.begin(walk);
+        // ========================================================= MMA: S
+        // The score products S = Q.K^T, tile by tile, each as soon as its
+        // page has landed, its S buffer has been read and (at the start of a
+        // unit) the query is in TMEM.  One elected lane of the converged
+        // warp issues them.
+        TileIter qk;
+        qk.begin(walk, pv);
         bool ok = !skip;
         bool issued = false;
-        uint64_t t_wait = 0;
-        bool waiting = false;
         const uint64_t dq0 = smem_desc(smem_u32(smem + OFF_STAGE), 16, 1024, SWZ_128B);
         const uint64_t dr0 = smem_desc(smem_u32(smem + OFF_STAGE + 4 * BOX_C_BYTES), 16, 512, SWZ_64B);
-        const uint64_t dp0 = smem_desc(smem_u32(smem + OFF_STAGE), BOX_C_BYTES, 1024, SWZ_128B);
-        while (ok && pvi.have) {
-            bool progress = false;
-            if (!qk.have || pvi.tile < qk.tile) {
-                const int b = pvi.buf();
-                bool ready = mbar_test(P_FULL(b), pvi.parity());
-                if (ready && pvi.first_in_seg() && pvi.seg > 0)
-                    ready = mbar_test(O_FREE, (uint32_t)((pvi.seg - 1) & 1));
-                if (__shfl_sync(0xffffffffu, ready, 0)) {
-                    tc_fence_after();
-                    if (elect_one_sync()) {
-                        // C as MN-major B: 64-column boxes 8 KB apart, 8-row
-                        // groups 1 KB apart, 16 tokens = 2 KB per step.
-                        const uint64_t db = dp0 + ((uint64_t)(pvi.stage() * STAGE_BYTES + pvi.t * (TILE * 128)) >> 4);
-                        const uint32_t acc0 = pvi.first_in_seg() ? 0u : 1u;
+        while (ok && qk.have) {
+            const int b = qk.buf();
+            if (qk.t == 0) ok = __all_sync(0xffffffffu, mbar_wait(FULL(qk.stage()), qk.page_parity(), 0x301));
+            if (ok && qk.tile >= 2) ok = __all_sync(0xffffffffu, mbar_wait(S_FREE(b), qk.parity(2), 0x302));
+            if (ok && qk.first_in_seg())
+                ok = __all_sync(0xffffffffu, mbar_wait(Q_FULL, (uint32_t)(qk.seg & 1), 0x303));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one_sync()) {
+                const uint32_t off = (uint32_t)(qk.stage() * STAGE_BYTES);
+                const uint64_t dc = dq0 + ((uint64_t)(off + qk.t * (TILE * 128)) >> 4);
+                const uint64_t dr = dr0 + ((uint64_t)(off + qk.t * (TILE * 64)) >> 4);
+                const uint32_t d = tmem + TM_S + 32 * b;
 #pragma unroll
-                        for (int k = 0; k < TILE / 16; ++k)
-                            mma_ts(tmem + TM_O, tmem + TM_P + 16 * b + 8 * k, db + (uint64_t)(k * 2048 >> 4),
-                                   IDESC_PV, k == 0 ? acc0 : 1u);
-                        tc_commit(PV_DONE(b));
-                        if (pvi.last_in_page()) tc_commit(EMPTY(pvi.stage()));
-                    }
-                    __syncwarp();
-                    pvi.advance();
-                    progress = true;
-                }
-            }
-            if (qk.have) {
-                const int b = qk.buf();
-                bool ready = qk.t != 0 || mbar_test(FULL(qk.stage()), qk.page_parity());
-                if (ready && qk.tile >= 2) ready = mbar_test(S_FREE(b), qk.parity(2));
-                if (ready && qk.first_in_seg()) ready = mbar_test(Q_FULL, (uint32_t)(qk.seg & 1));
-                if (__shfl_sync(0xffffffffu, ready, 0)) {
-                    tc_fence_after();
-                    if (elect_one_sync()) {
-                        const uint32_t off = (uint32_t)(qk.stage() * STAGE_BYTES);
-                        const uint64_t dc = dq0 + ((uint64_t)(off + qk.t * (TILE * 128)) >> 4);
-                        const uint64_t dr = dr0 + ((uint64_t)(off + qk.t * (TILE * 64)) >> 4);
-                        const uint32_t d = tmem + TM_S + 32 * b;
+                for (int k = 0; k < 16; ++k)  // latent features, K-major SW128
+                    mma_ts(d, tmem + TM_Q + 8 * k, dc + (uint64_t)(((k / 4) * BOX_C_BYTES + (k % 4) * 32) >> 4),
+                           IDESC_QK, k > 0 ? 1u : 0u);
 #pragma unroll
-                        for (int k = 0; k < 16; ++k)  // latent features, K-major SW128
-                            mma_ts(d, tmem + TM_Q + 8 * k,
-                                   dc + (uint64_t)(((k / 4) * BOX_C_BYTES + (k % 4) * 32) >> 4), IDESC_QK,
-                                   k > 0 ? 1u : 0u);
-#pragma unroll
-                        for (int k = 0; k < 2; ++k)  // RoPE features, K-major SW64
-                            mma_ts(d, tmem + TM_Q + 128 + 8 * k, dr + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
-                        tc_commit(S_FULL(b));
-                    }
-                    __syncwarp();
-                    issued = true;
-                    qk.advance();
-                    progress = true;
-                }
+                for (int k = 0; k < 2; ++k)  // RoPE features, K-major SW64
+                    mma_ts(d, tmem + TM_Q + 128 + 8 * k, dr + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
+                tc_commit(S_FULL(b));
             }
-            if (progress) {
-                waiting = false;
-            } else if (!waiting) {
-                waiting = true;
-                t_wait = global_timer_ns();
-            } else {
-                bool give_up = device_status_raised();
-                if (!give_up && global_timer_ns() - t_wait > MLA_WAIT_LIMIT_NS) {
-                    if (lane == 0) raise_device_status(MLA_DEV_TIMEOUT, 0x301u | ((blockIdx.x & 0xFFFu) << 12));
-                    give_up = true;
-                }
-                ok = !__shfl_sync(0xffffffffu, give_up, 0);
-            }
+            __syncwarp();
+            issued = true;
+            qk.advance(pv);
         }
         if (!ok && issued) {  // wait for the tensor core before TMEM goes away
-            if (elect_one_sync()) tc_commit(DRAIN);
+            if (elect_one_sync()) tc_commit(DRAIN(0));
             __syncwarp();
-            mbar_wait_teardown(DRAIN, 0, MLA_WAIT_LIMIT_NS);
+            mbar_wait_teardown(DRAIN(0), 0, MLA_WAIT_LIMIT_NS);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ========================================================= MMA: O
+        // O += P.C, tile by tile in order (one issuing thread, so the
+        // products land in tile order and every call gives the same bits),
+        // each as soon as its P is in TMEM and, for a unit's first tile
+        // (which overwrites O), once the last unit's epilogue has read O.
+        TileIter it;
+        it.begin(walk, pv);
+        bool ok = !skip;
+        bool issued = false;
+        const uint64_t dp0 = smem_desc(smem_u32(smem + OFF_STAGE), BOX_C_BYTES, 1024, SWZ_128B);
+        while (ok && it.have) {
+            const int b = it.buf();
+            ok = __all_sync(0xffffffffu, mbar_wait(P_FULL(b), it.parity(), 0x401));
+            if (ok && it.first_in_seg() && it.seg > 0)
+                ok = __all_sync(0xffffffffu, mbar_wait(O_FREE, (uint32_t)((it.seg - 1) & 1), 0x402));
+            if (!ok) break;
+            tc_fence_after();
+            if (elect_one_sync()) {
+                // C as MN-major B: 64-column boxes 8 KB apart, 8-row
+                // groups 1 KB apart, 16 tokens = 2 KB per step.
+                const uint64_t db = dp0 + ((uint64_t)(it.stage() * STAGE_BYTES + it.t * (TILE * 128)) >> 4);
+                const uint32_t acc0 = it.first_in_seg() ? 0u : 1u;
+#pragma unroll
+                for (int k = 0; k < TILE / 16; ++k)
+                    mma_ts(tmem + TM_O, tmem + TM_P + 16 * b + 8 * k, db + (uint64_t)(k * 2048 >> 4), IDESC_PV,
+                           k == 0 ? acc0 : 1u);
+                tc_commit(PV_DONE(b));
+                if (it.last_in_page()) tc_commit(EMPTY(it.stage()));
+            }
+            __syncwarp();
+            issued = true;
+            it.advance(pv);
+        }
+        if (!ok && issued) {  // wait for the tensor core before TMEM goes away
+            if (elect_one_sync()) tc_commit(DRAIN(1));
+            __syncwarp();
+            mbar_wait_teardown(DRAIN(1), 0, MLA_WAIT_LIMIT_NS);
         }
         __syncwarp();
     } else {
         // ===================================================== tile groups
+        // A group's tiles are software-pipelined: the front half of its next
+        // tile (query if a unit starts there, own partial scores out of TMEM
+        // and off to the peer) runs before the back half of its current one
+        // (the peer's partial in, softmax, P, epilogue), so the exchange of
+        // one tile overlaps the softmax of the one before.
         const int grp = (warp - WG_WARP0) / 4;  // tiles with index % 2 == grp
-        const int b = grp;                      // their S, P, X buffers and barriers
+        const int b = grp;                      // their S and P buffers and barriers
         const int q4 = warp & 3;
         const int h = q4 * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
-        const uint32_t peer_x = map_to_rank(smem_u32(smem + OFF_X + b * XT_BYTES), peer);
-        const uint32_t peer_xfull = map_to_rank(XFULL(b), peer);
+        const uint32_t peer_x0 = map_to_rank(smem_u32(smem + OFF_X + 2 * grp * XT_BYTES), peer);
+        const uint32_t peer_xfull0 = map_to_rank(XFULL(2 * grp), peer);
         float* pub = reinterpret_cast<float*>(smem + OFF_PUB);  // [2][3][HEADS]
         const bool leader = warp == WG_WARP0 + 4 * grp && lane == 0;
-        TileIter it;
-        it.begin(walk);
+        const int my_g = (int)g_id;
+        auto xslot = [](int64_t i) { return (int)((i >> 1) & 1); };
+        auto xpar = [](int64_t i) { return (uint32_t)((i >> 2) & 1); };
         bool ok = !skip;
         float m_ref = -INFINITY, l_part = 0.f;  // this group's row sum, relative to m_ref
         int64_t my_seg = -1;
         int64_t armed = misc[7 + grp], consumed = 0;
-        while (ok && it.have) {
-            if ((it.tile & 1) != grp) {
-                it.advance();
-                continue;
-            }
-            const int64_t i = it.tile;
-            const bool first = it.first_in_seg();
-            if (my_seg != it.seg) {  // a new unit piece: this group's sums restart
-                my_seg = it.seg;
-                m_ref = -INFINITY;
-                l_part = 0.f;
-            }
-            if (first) {
+
+        uint32_t own_c[TILE], own_n[TILE];  // partial scores of the current / next tile
+
+        // ---- front half of tile `t`; own_n receives its partial scores
+        auto front = [&](const TileIter& t) -> bool {
+            const int64_t i = t.tile;
+            if (t.first_in_seg()) {
                 // The query of this unit replaces the last one once every
                 // score product of the tile before has completed.
-                if (i >= 1) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(S_FULL(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x501));
-                    if (!ok) break;
-                }
-                const Unit& un = it.sg.un;
-                const int head = un.hg * HEADS + h;
+                if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(S_FULL(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x501)))
+                    return false;
+                const int bt = t.sg.u / p.HG;  // unit u = (b * T + t) * HG + hg
+                const int head = (t.sg.u - bt * p.HG) * HEADS + h;
                 const bool live = head < p.H;
-                const int64_t qrow = ((int64_t)un.b * p.T + un.t) * p.H + head;
+                const int64_t qrow = (int64_t)bt * p.H + head;
                 const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat + qrow * DC + rank * HALF_C);
                 const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * DR + rank * HALF_R);
 #pragma unroll
@@ -690,69 +715,77 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(Q_FULL);
             }
-            // ---- own partial scores: TMEM -> registers -> the peer
-            ok = __all_sync(0xffffffffu, mbar_wait(S_FULL(b), it.parity(), 0x502));
-            if (!ok) break;
+            if (!__all_sync(0xffffffffu, mbar_wait(S_FULL(b), t.parity(), 0x502))) return false;
             tc_fence_after();
-            uint32_t own[TILE];
-            tmem_ld32(trow + TM_S + 32 * b, own);
+            uint32_t r[TILE];
+            tmem_ld32(trow + TM_S + 32 * b, r);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(S_FREE(b));
-            if (i >= 2) {  // the peer has read our copy of the tile two back
-                ok = __all_sync(0xffffffffu, mbar_wait(XFREE(b), it.parity(2), 0x503));
-                if (!ok) break;
-            }
+            // our copy of this group's tile four back has been read by the peer
+            if (i >= 4 && !__all_sync(0xffffffffu, mbar_wait(XFREE(2 * grp + xslot(i)), xpar(i - 4), 0x503)))
+                return false;
+            const uint32_t dst = peer_x0 + (uint32_t)xslot(i) * XT_BYTES;
+            const uint32_t pbar = peer_xfull0 + 8u * (uint32_t)xslot(i);
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k)
-                st_async_v4(peer_x + (uint32_t)(k * HEADS + h) * 16u, own[4 * k], own[4 * k + 1], own[4 * k + 2],
-                            own[4 * k + 3], peer_xfull);
-            // ---- plus the peer's partial, from X[b]
-            ok = __all_sync(0xffffffffu, mbar_wait<true>(XFULL(b), it.parity(), 0x504));
-            if (!ok) break;
-            consumed = i + 1;
-            if (leader && i + 2 < n_tiles) {
-                mbar_arrive_expect_tx(XFULL(b), XT_BYTES);  // X[b] next receives tile i + 2
-                armed = i + 3;
+                st_async_v4(dst + (uint32_t)(k * HEADS + h) * 16u, r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3], pbar);
+#pragma unroll
+            for (int k = 0; k < TILE; ++k) own_n[k] = r[k];
+            return true;
+        };
+
+        // ---- back half of tile `c`, whose own partial scores are in own_c
+        auto back = [&](const TileInfo& c) -> bool {
+            const int64_t i = c.tile;
+            if (my_seg != c.seg) {  // a new unit piece: this group's sums restart
+                my_seg = c.seg;
+                m_ref = -INFINITY;
+                l_part = 0.f;
             }
-            const float4* xp = reinterpret_cast<const float4*>(smem + OFF_X + b * XT_BYTES);
-            const int valid = it.valid();
+            const int x = 2 * grp + xslot(i);
+            if (!__all_sync(0xffffffffu, mbar_wait<true>(XFULL(x), xpar(i), 0x504))) return false;
+            consumed = i + 1;
+            if (leader && i + 4 < n_tiles) {
+                mbar_arrive_expect_tx(XFULL(x), XT_BYTES);  // this buffer next receives tile i + 4
+                armed = i + 5;
+            }
+            const float4* xp = reinterpret_cast<const float4*>(smem + OFF_X + x * XT_BYTES);
             float s[TILE];
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k) {
-                const float4 c = xp[k * HEADS + h];
-                s[4 * k] = (__uint_as_float(own[4 * k]) + c.x) * p.scale_log2;
-                s[4 * k + 1] = (__uint_as_float(own[4 * k + 1]) + c.y) * p.scale_log2;
-                s[4 * k + 2] = (__uint_as_float(own[4 * k + 2]) + c.z) * p.scale_log2;
-                s[4 * k + 3] = (__uint_as_float(own[4 * k + 3]) + c.w) * p.scale_log2;
+                const float4 v = xp[k * HEADS + h];
+                s[4 * k] = (__uint_as_float(own_c[4 * k]) + v.x) * p.scale_log2;
+                s[4 * k + 1] = (__uint_as_float(own_c[4 * k + 1]) + v.y) * p.scale_log2;
+                s[4 * k + 2] = (__uint_as_float(own_c[4 * k + 2]) + v.z) * p.scale_log2;
+                s[4 * k + 3] = (__uint_as_float(own_c[4 * k + 3]) + v.w) * p.scale_log2;
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < TILE; ++j) {
-                if (j >= valid) s[j] = -INFINITY;
+                if (j >= c.valid) s[j] = -INFINITY;
                 mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
             }
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             // ---- the running maximum after the tile before (the other group)
             float m_prev = -INFINITY;
             if (i >= 1) {
-                ok = __all_sync(0xffffffffu, mbar_wait(M_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x505));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(M_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x505)))
+                    return false;
                 m_prev = pub[(b ^ 1) * 3 * HEADS + h];
             }
-            const bool last = it.last_in_seg();
             float m_oth = -INFINITY, l_oth = 0.f;  // the other group's sums (unit's last tile only)
-            if (last && !first) {
+            if (c.last && !c.first) {
                 // before this tile's maximum is published, so that the other
                 // group cannot publish its next tile's sums over these
-                ok = __all_sync(0xffffffffu, mbar_wait(L_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x506));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(L_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x506)))
+                    return false;
                 m_oth = pub[((b ^ 1) * 3 + 1) * HEADS + h];
                 l_oth = pub[((b ^ 1) * 3 + 2) * HEADS + h];
             }
             float m_used;
             bool need = false;
-            if (first) {
+            if (c.first) {
                 m_used = mx;
             } else {
                 need = mx > m_prev + RESCALE_THRESHOLD;
@@ -760,18 +793,19 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             }
             if (__any_sync(0xffffffffu, need)) {
                 // O moves to the new maximum once the tile before has been
-                // added to it, and before any later tile is
-                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x507));
-                if (!ok) break;
+                // added to it (and with it every earlier one: the products
+                // land in tile order), and before any later tile is
+                if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x507)))
+                    return false;
                 tc_fence_after();
                 const float alpha = ex2(m_prev - m_used);
 #pragma unroll 1
-                for (int c = 0; c < HALF_C; c += 32) {
+                for (int cc = 0; cc < HALF_C; cc += 32) {
                     uint32_t r[32];
-                    tmem_ld32(trow + TM_O + c, r);
+                    tmem_ld32(trow + TM_O + cc, r);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
-                    tmem_st32(trow + TM_O + c, r);
+                    tmem_st32(trow + TM_O + cc, r);
                 }
                 tmem_st_wait();
                 tc_fence_before();
@@ -785,8 +819,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             }
             // ---- P[b] is free once the tile two back has been multiplied
             if (i >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b), it.parity(2), 0x508));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)(((i - 2) >> 1) & 1), 0x508)))
+                    return false;
                 tc_fence_after();
             }
             {
@@ -810,28 +844,27 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             if (lane == 0) {
                 mbar_arrive(P_FULL(b));
                 mbar_arrive(L_PUB(b));
-                // Every value read from X[b] has gone into P, now stored.
-                mbar_arrive_remote_relaxed(map_to_rank(XFREE(b), peer));
+                // Every value read from this X buffer has gone into P, now stored.
+                mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));
             }
-            if (last) {
+            if (c.last) {
                 // ---- epilogue: O / l of this CTA's 256 columns, lse
-                const Segment& sg = it.sg;
-                ok = __all_sync(0xffffffffu, mbar_wait(PV_DONE(b), it.parity(), 0x509));
-                if (!ok) break;
+                if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)((i >> 1) & 1), 0x509))) return false;
                 tc_fence_after();
-                const float l = l_part + (first ? 0.f : l_oth * ex2(m_oth - m_used));
-                const int head = sg.un.hg * HEADS + h;
+                const float l = l_part + (c.first ? 0.f : l_oth * ex2(m_oth - m_used));
+                const int bt = c.u / p.HG;  // unit u = (b * T + t) * HG + hg
+                const int head = (c.u - bt * p.HG) * HEADS + h;
                 const bool live = head < p.H;
-                const int64_t qrow = ((int64_t)sg.un.b * p.T + sg.un.t) * p.H + head;
+                const int64_t qrow = (int64_t)bt * p.H + head;
                 const float inv_l = 1.f / l;
-                if (sg.slot < 0) {
+                if (c.slot < 0) {
                     __nv_bfloat16* dst = p.o + qrow * DC + rank * HALF_C;
 #pragma unroll 1
-                    for (int c = 0; c < HALF_C; c += 32) {
+                    for (int cc = 0; cc < HALF_C; cc += 32) {
                         uint32_t r[32];
-                        tmem_ld32(trow + TM_O + c, r);
+                        tmem_ld32(trow + TM_O + cc, r);
                         if (live) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
                             for (int v = 0; v < 4; ++v)
                                 d4[v] = make_uint4(
@@ -843,42 +876,74 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     }
                     if (live && rank == 0) p.lse[qrow] = (m_used + __log2f(l)) * LN2;
                 } else {
-                    float* dst = p.ws_o + (sg.slot * HEADS + h) * DC + rank * HALF_C;
+                    float* dst = p.ws_o + (c.slot * HEADS + h) * DC + rank * HALF_C;
 #pragma unroll 1
-                    for (int c = 0; c < HALF_C; c += 32) {
+                    for (int cc = 0; cc < HALF_C; cc += 32) {
                         uint32_t r[32];
-                        tmem_ld32(trow + TM_O + c, r);
-                        float4* d4 = reinterpret_cast<float4*>(dst + c);
+                        tmem_ld32(trow + TM_O + cc, r);
+                        float4* d4 = reinterpret_cast<float4*>(dst + cc);
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
                             d4[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
                                                 __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
                     }
-                    if (rank == 0) p.ws_lse[sg.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
+                    if (rank == 0) p.ws_lse[c.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
                 }
-                if (rank == 0 && h == 0 && sg.g_first == walk.g)
-                    p.ws_unit[sg.u] = make_int2((int)sg.g_first, (int)sg.g_last);
+                if (rank == 0 && h == 0 && c.g_first == my_g)
+                    p.ws_unit[c.u] = make_int2((int)c.g_first, c.g_last);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(O_FREE);
             }
-            it.advance();
+            return true;
+        };
+
+        TileIter it;
+        it.begin(walk, pv);
+        if (it.have && (it.tile & 1) != grp) it.advance(pv);  // this group's first tile
+        TileInfo cur;
+        bool have_cur = false;
+        if (ok && it.have) {
+            ok = front(it);
+#pragma unroll
+            for (int k = 0; k < TILE; ++k) own_c[k] = own_n[k];
+            cur.set(it);
+            have_cur = true;
+            it.advance(pv);
+            if (it.have) it.advance(pv);
+        }
+        // `it` now points at the group's next tile: its front half runs
+        // before the back half of `cur`.
+        while (ok && have_cur) {
+            if (it.have) {
+                ok = front(it);
+                if (!ok) break;
+            }
+            ok = back(cur);
+            if (!ok || !it.have) break;
+            cur.set(it);
+#pragma unroll
+            for (int k = 0; k < TILE; ++k) own_c[k] = own_n[k];
+            it.advance(pv);
+            if (it.have) it.advance(pv);
         }
         if (leader) {
             misc[7 + grp] = armed;
             misc[9 + grp] = consumed;
         }
+
     }
 
     tc_fence_before();
     __syncthreads();
-    // Teardown: a partial S tile the peer may still be copying into X lands
+    // Teardown: partial S tiles the peer may still be copying into X land
     // before this CTA's shared memory can go away (only after an abort can
-    // one be armed but not consumed; the wait gives up after 10 ms).
+    // one be armed but not consumed; each wait gives up after 10 ms).
     if (threadIdx.x == 0) {
         for (int g = 0; g < 2; ++g)
-            if (misc[7 + g] > misc[9 + g])
-                mbar_wait_teardown(XFULL(g), (uint32_t)(((misc[7 + g] - 1) >> 1) & 1), 10000000ull);
+            for (int64_t t = misc[9 + g]; t < misc[7 + g]; ++t)
+                if ((t & 1) == g)
+                    mbar_wait_teardown(XFULL((int)(2 * g + ((t >> 1) & 1))), (uint32_t)((t >> 2) & 1), 10000000ull);
     }
     if (warp == 1) tmem_dealloc(tmem, TM_COLS);
     cluster_sync();

@@ -129,19 +129,19 @@ mla_status_t launch_status(int n = 1) {
 // Does the plan cut some unit between clusters, or leave one without any
 // visible position?  (Only then is the combine kernel needed.)
 bool host_plan_needs_combine(const int32_t* lens, int B, int T, int HG, int max_pages, int causal,
-                             int64_t launched) {
+                             int launched) {
     mla::dec::PlanView v{lens, B, T, HG, max_pages, causal};
-    const int64_t U = (int64_t)B * T * HG;
-    int64_t total = 0;
-    for (int64_t u = 0; u < U; ++u) {
+    const int U = B * T * HG;
+    int total = 0;
+    for (int u = 0; u < U; ++u) {
         const mla::dec::Unit un = mla::dec::unit_of(v, u);
         if (un.pages == 0 || un.bad_len) return true;
         total += un.pages;
     }
-    const int64_t G = mla::dec::clusters_used(total, launched);
-    int64_t pos = 0;
-    for (int64_t u = 0; u < U; ++u) {
-        const int64_t n = mla::dec::unit_of(v, u).pages;
+    const int G = mla::dec::clusters_used(total, launched);
+    int pos = 0;
+    for (int u = 0; u < U; ++u) {
+        const int n = mla::dec::unit_of(v, u).pages;
         if (mla::dec::cluster_of_page(pos, total, G) != mla::dec::cluster_of_page(pos + n - 1, total, G))
             return true;
         pos += n;
@@ -410,12 +410,13 @@ int64_t mla_decode_plan(const int32_t* seq_lens_host, int B, int T, int H, int m
         clusters = di.decode_clusters;
     }
     const int HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
+    if (!mla::dec::plan_fits_int32(B, T, HG, max_pages)) return -1;
     mla::dec::PlanView v{seq_lens_host, B, T, HG, max_pages, causal ? 1 : 0};
     int64_t n = 0;
-    for (int64_t g = 0; g < clusters; ++g) {
+    for (int g = 0; g < clusters; ++g) {
         mla::dec::Walker w = mla::dec::host_walker(v, clusters, g);
         mla::dec::Segment sg;
-        while (w.next(sg)) {
+        while (w.next(v, sg)) {
             if (n < cap) {
                 int64_t* r = out + 7 * n;
                 r[0] = g;
@@ -460,9 +461,10 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     if (d_c != mla::dec::DC || d_r != mla::dec::DR || page_size != mla::dec::PAGE)
         return MLA_ERR_UNSUPPORTED;
     if (num_pages * mla::dec::PAGE > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+    const int HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
+    if (!mla::dec::plan_fits_int32(B, T, HG, max_pages)) return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const int HG = (H + mla::dec::HEADS - 1) / mla::dec::HEADS;
     const int64_t U = (int64_t)B * T * HG;
     const int64_t G = di.decode_clusters;
     const DecodeWs wl = decode_ws_layout(U, G, d_c);
