@@ -206,6 +206,38 @@ mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail);
  */
 void mla_set_decode_events(void* start, void* end);
 
+/*
+ * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot
+ * allocate device memory: a host that owns all of the GPU's memory and
+ * hands this library only its inputs and outputs (an inference-server
+ * plugin with a fixed memory budget, for instance), or a code path that
+ * must not allocate because allocation could block or synchronise the
+ * device.  It takes the same arguments as mla_decode_attn without the
+ * workspace, computes the same result with the same kernels, and allocates
+ * nothing: its scratch is a fixed array of mla_decode_noalloc_max_bytes()
+ * bytes inside the library, which every GPU that loads the library holds
+ * until the process exits.  (The web pages on MLA have no counterpart to
+ * this call; it is an interface convenience.)
+ *
+ * The first call on a device looks up that array's device address (once
+ * per device, with the device current); make that first call before any
+ * stream capture.  Every call shares the one array and overwrites what the
+ * last call left there, so calls whose kernels overlap on the GPU (on
+ * different streams, or from different host threads) race: serialise them.
+ * A shape whose scratch (mla_decode_workspace_size) exceeds the maximum
+ * returns MLA_ERR_UNSUPPORTED before anything is launched; use
+ * mla_decode_attn with a caller-owned workspace for it.
+ */
+mla_status_t mla_decode_attn_noalloc(const void* q_lat, const void* q_pe, const void* kv_pool,
+                                     const int32_t* page_table, const int32_t* seq_lens,
+                                     const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                                     int d_r, int page_size, int max_pages, int64_t num_pages,
+                                     float scale, int causal, void* o, float* lse,
+                                     mla_dtype_t dtype, mla_stream_t stream);
+
+/* Size in bytes of the fixed scratch array of mla_decode_attn_noalloc. */
+size_t mla_decode_noalloc_max_bytes(void);
+
 /* Number of kernels this library has launched in this process so far. */
 uint64_t mla_launch_count(void);
 

@@ -513,4 +513,66 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     return launch_status();
 }
 
+// ----------------------------------------------- mla_decode_attn_noalloc
+
+}  // extern "C"
+
+namespace {
+
+// Scratch for mla_decode_attn_noalloc: a fixed array in device memory that
+// the CUDA runtime sets aside on every GPU that loads this library, for as
+// long as the process lives.  Calls share it and it keeps the last call's
+// contents (the decode scratch needs no initial value).
+constexpr size_t kNoallocScratchBytes = size_t(48) << 20;
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoallocScratchBytes];
+
+// Device address of g_decode_scratch on each device, looked up once per
+// device (with that device current).  In host code the array's name is only
+// a stand-in for the symbol, never a device address.
+void* g_scratch_addr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+void* decode_scratch_address() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_scratch_addr[dev] = ptr;
+    }
+    return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mla_decode_noalloc_max_bytes(void) { return kNoallocScratchBytes; }
+
+mla_status_t mla_decode_attn_noalloc(const void* q_lat, const void* q_pe, const void* kv_pool,
+                                     const int32_t* page_table, const int32_t* seq_lens,
+                                     const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                                     int d_r, int page_size, int max_pages, int64_t num_pages,
+                                     float scale, int causal, void* o, float* lse,
+                                     mla_dtype_t dtype, mla_stream_t stream) {
+    if (!q_lat || !q_pe || !kv_pool || !page_table || !seq_lens || !o || !lse)
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (B < 1 || T < 1 || H < 1 || d_c < 1) return MLA_ERR_INVALID_ARG;
+    const size_t need = mla_decode_workspace_size(B, T, H, d_c, dtype);
+    if (need > kNoallocScratchBytes) return MLA_ERR_UNSUPPORTED;
+    void* scratch = nullptr;
+    if (need > 0) {
+        scratch = decode_scratch_address();
+        if (!scratch) return MLA_ERR_CUDA;
+    }
+    return mla_decode_attn(q_lat, q_pe, kv_pool, page_table, seq_lens, seq_lens_host, B, T, H, d_c,
+                           d_r, page_size, max_pages, num_pages, scale, causal, o, lse, scratch,
+                           need > 0 ? kNoallocScratchBytes : 0, dtype, stream);
+}
+
 }  // extern "C"

@@ -25,7 +25,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_combine_splits",
            "mla_out_proj_workspace_size", "mla_out_proj", "mla_get_device_status",
            "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count",
-           "mla_decode_plan"]
+           "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes"]
 
 
 class MLAError(RuntimeError):
@@ -72,6 +72,11 @@ def _lib():
         lib.mla_launch_count.restype = ctypes.c_uint64
         lib.mla_decode_plan.argtypes = [P, I, I, I, I, I, I, P, L]
         lib.mla_decode_plan.restype = L
+        lib.mla_decode_attn_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, L, F, I, P,
+                                                P, I, P]
+        lib.mla_decode_attn_noalloc.restype = I
+        lib.mla_decode_noalloc_max_bytes.argtypes = []
+        lib.mla_decode_noalloc_max_bytes.restype = Z
         _LIB = lib
     return _LIB
 
@@ -153,6 +158,36 @@ def decode_attn(q_lat, q_pe, kv_pool, page_table, seq_lens, scale: float, causal
         d_c, d_r, page, max_pages, num_pages, float(scale), int(bool(causal)), _ptr(o), _ptr(lse),
         _ptr(workspace), ws_bytes, dt, _stream(stream)))
     return o, lse
+
+
+def decode_attn_noalloc(q_lat, q_pe, kv_pool, page_table, seq_lens, scale: float,
+                        causal: bool = False, o=None, lse=None, seq_lens_host=None, stream=None):
+    """decode_attn through mla_decode_attn_noalloc: the same result, with the
+    library's fixed internal scratch instead of a caller workspace (for
+    callers that cannot allocate device memory; the caller still provides
+    inputs and outputs).  Returns (o, lse)."""
+    B, T, H, d_c = q_lat.shape
+    d_r = q_pe.shape[3]
+    num_pages, page, width = kv_pool.shape
+    max_pages = page_table.shape[1]
+    if o is None:
+        o = torch.empty_like(q_lat)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q_lat.device)
+    host = None
+    if seq_lens_host is not None:
+        seq_lens_host = seq_lens_host.to(torch.int32).contiguous()
+        host = ctypes.c_void_p(seq_lens_host.data_ptr())
+    _check("mla_decode_attn_noalloc", _lib().mla_decode_attn_noalloc(
+        _ptr(q_lat), _ptr(q_pe), _ptr(kv_pool), _ptr(page_table), _ptr(seq_lens), host, B, T, H,
+        d_c, d_r, page, max_pages, num_pages, float(scale), int(bool(causal)), _ptr(o), _ptr(lse),
+        _dt(q_lat), _stream(stream)))
+    return o, lse
+
+
+def noalloc_max_bytes() -> int:
+    """Size of the fixed scratch array behind decode_attn_noalloc."""
+    return int(_lib().mla_decode_noalloc_max_bytes())
 
 
 def combine_splits(o_part, lse_part, o=None, lse=None, out_dtype=torch.bfloat16, stream=None):
