@@ -80,7 +80,9 @@ def work_of(case: workloads.DecodeCase):
 
 
 class ClockSampler:
-    """Polls NVML (SM clock, max clock, throttle reasons) in a thread."""
+    """SM clock and throttle reasons sampled during the timed region: through
+    NVML when the Python binding is importable, else by an nvidia-smi process
+    polling every 50 ms."""
 
     REASONS = {
         "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
@@ -88,9 +90,11 @@ class ClockSampler:
     }
 
     def __init__(self, device_index: int):
-        self.samples, self.reasons, self.ok = [], set(), False
+        self.samples, self.reasons = [], set()
         self.err = ""
         self.max_mhz = None
+        self.mode = None
+        self.device_index = device_index
         try:
             import pynvml
             pynvml.nvmlInit()
@@ -101,13 +105,15 @@ class ClockSampler:
                 self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
             self.nv = pynvml
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception as e:  # pragma: no cover - no NVML
+            self.mode = "nvml"
+        except Exception as e:
             self.err = repr(e)
-            self.ok = False
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "smi"
         self._stop = threading.Event()
 
-    def _run(self):
+    def _run_nvml(self):
         while not self._stop.is_set():
             try:
                 self.samples.append(self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM))
@@ -120,22 +126,49 @@ class ClockSampler:
             time.sleep(0.002)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "smi":
+            import subprocess
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+            idx = vis.split(",")[self.device_index] if vis else str(self.device_index)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", idx, "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)  # let the first sample land before the timed work starts
         return self
 
     def __exit__(self, *exc):
         self._stop.set()
-        if self.ok:
+        if self.mode == "nvml":
             self.t.join()
+        elif self.mode == "smi":
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            for line in out.splitlines():
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 3:
+                    continue
+                try:
+                    self.samples.append(float(parts[0]))
+                    self.max_mhz = float(parts[1])
+                    mask = int(parts[2], 16)
+                except ValueError:
+                    continue
+                for name, bit in self.REASONS.items():
+                    if mask & bit:
+                        self.reasons.add(name)
 
     def summary(self):
-        if not self.ok or not self.samples:
+        if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "note": "no NVML samples: " + getattr(self, "err", "")}
+                    "note": "no clock samples: " + self.err}
         return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+                "reasons": sorted(self.reasons), "samples": len(self.samples),
+                "source": self.mode}
 
 
 def dist_setup():

@@ -949,51 +949,71 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     cluster_sync();
 }
 
-// Merge the partial slots of split units (grid: U * 128 blocks of 128
-// threads, one head row each); also writes o = 0, lse = -inf for units that
-// see no cached position.
-__global__ void __launch_bounds__(128)
+// Merge the partial results of units cut between clusters.  One warp per
+// head row (8 rows per 256-thread block): lane k < pieces reads piece k's
+// lse, the warp forms the log-sum-exp weights with shuffles, and each lane
+// then merges 16 of the row's 512 columns from every piece.  Also writes
+// o = 0, lse = -inf for units that see no cached position.
+constexpr int COMBINE_ROWS = 8;
+
+__global__ void __launch_bounds__(32 * COMBINE_ROWS)
 decode_combine_kernel(const Params p) {
     if (device_status_raised()) return;
-    const int64_t u = blockIdx.x / HEADS;
-    const int h = blockIdx.x % HEADS;
-    PlanView pv;
-    pv.seq_lens = p.seq_lens;
-    pv.B = p.B;
-    pv.T = p.T;
-    pv.HG = p.HG;
-    pv.max_pages = p.max_pages;
-    pv.causal = p.causal;
-    const Unit un = unit_of(pv, u);
-    const int head = un.hg * HEADS + h;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int row = blockIdx.x * COMBINE_ROWS + warp;  // u * HEADS + h
+    const int u = row / HEADS, h = row % HEADS;
+    if (u >= p.B * p.T * p.HG) return;
+    const int bt = u / p.HG;  // unit u = (b * T + t) * HG + hg
+    const int head = (u - bt * p.HG) * HEADS + h;
     if (head >= p.H) return;
-    const int64_t qrow = ((int64_t)un.b * p.T + un.t) * p.H + head;
-    const int c = 4 * threadIdx.x;
-    __nv_bfloat16* dst = p.o + qrow * DC + c;
+    const PlanView pv{p.seq_lens, p.B, p.T, p.HG, p.max_pages, p.causal};
+    const int2 gg = p.ws_unit[u];         // issued together with the length read below
+    const Unit un = unit_of(pv, u);
+    const int64_t qrow = (int64_t)bt * p.H + head;
+    __nv_bfloat16* dst = p.o + qrow * DC + 16 * lane;
     if (un.pages == 0) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(0u, 0u);
-        if (threadIdx.x == 0) p.lse[qrow] = -INFINITY;
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(0u, 0u, 0u, 0u);
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (lane == 0) p.lse[qrow] = -INFINITY;
         return;
     }
-    const int2 gg = p.ws_unit[u];
     if (gg.x == gg.y) return;  // written directly by the attention kernel
+    const int n = gg.y - gg.x + 1;
     float m = -INFINITY;
-    for (int g = gg.x; g <= gg.y; ++g) m = fmaxf(m, p.ws_lse[(g + u) * HEADS + h]);
+    for (int k = lane; k < n; k += 32) m = fmaxf(m, p.ws_lse[(int64_t)(gg.x + k + u) * HEADS + h]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float sum = 0.f;
-    for (int g = gg.x; g <= gg.y; ++g) sum += __expf(p.ws_lse[(g + u) * HEADS + h] - m);
+    for (int k = lane; k < n; k += 32) sum += __expf(p.ws_lse[(int64_t)(gg.x + k + u) * HEADS + h] - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float L = m + __logf(sum);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int g = gg.x; g <= gg.y; ++g) {
-        const int64_t slot = g + u;
-        const float w = __expf(p.ws_lse[slot * HEADS + h] - L);
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * HEADS + h) * DC + c));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    float acc[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) acc[j] = 0.f;
+    for (int k0 = 0; k0 < n; k0 += 32) {
+        const int kk = k0 + lane;
+        const float w_l = kk < n ? __expf(p.ws_lse[(int64_t)(gg.x + kk + u) * HEADS + h] - L) : 0.f;
+        const int cnt = n - k0 < 32 ? n - k0 : 32;
+        for (int k = 0; k < cnt; ++k) {
+            const float w = __shfl_sync(0xffffffffu, w_l, k);
+            const float4* src = reinterpret_cast<const float4*>(
+                p.ws_o + ((int64_t)(gg.x + k0 + k + u) * HEADS + h) * DC + 16 * lane);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const float4 x = __ldcg(src + v);
+                acc[4 * v] = fmaf(w, x.x, acc[4 * v]);
+                acc[4 * v + 1] = fmaf(w, x.y, acc[4 * v + 1]);
+                acc[4 * v + 2] = fmaf(w, x.z, acc[4 * v + 2]);
+                acc[4 * v + 3] = fmaf(w, x.w, acc[4 * v + 3]);
+            }
+        }
     }
-    *reinterpret_cast<uint2*>(dst) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-    if (threadIdx.x == 0) p.lse[qrow] = L;
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                                  pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+    if (lane == 0) p.lse[qrow] = L;
 }
 
 }  // namespace dec

@@ -509,7 +509,9 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     if (seq_lens_host &&
         !host_plan_needs_combine(seq_lens_host, B, T, HG, max_pages, p.causal, G))
         return MLA_OK;
-    mla::dec::decode_combine_kernel<<<(unsigned)(U * mla::dec::HEADS), 128, 0, st>>>(p);
+    mla::dec::decode_combine_kernel<<<(unsigned)((U * mla::dec::HEADS + mla::dec::COMBINE_ROWS - 1) /
+                                                 mla::dec::COMBINE_ROWS),
+                                      32 * mla::dec::COMBINE_ROWS, 0, st>>>(p);
     return launch_status();
 }
 
