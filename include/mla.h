@@ -202,7 +202,9 @@ mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail);
  * just after it, so that a caller can time that kernel apart from the
  * combine kernel of the same call.  Arguments are CUDA events (cudaEvent_t)
  * owned by the caller; NULL, NULL clears the hook.  Process-wide, not
- * thread-safe against concurrent decode calls.
+ * thread-safe against concurrent decode calls.  Under stream capture the
+ * events are recorded as external event nodes, so each replay of the graph
+ * records them.
  */
 void mla_set_decode_events(void* start, void* end);
 

@@ -501,11 +501,19 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     p.causal = causal ? 1 : 0;
 
     cudaEvent_t ev0 = g_ev_start, ev1 = g_ev_end;
-    if (ev0 && ev1 && cudaEventRecord(ev0, st) != cudaSuccess) return MLA_ERR_CUDA;
+    // Inside a stream capture an event record only orders the graph unless it
+    // is recorded as external; then replaying the graph records it.
+    unsigned ev_flags = cudaEventRecordDefault;
+    if (ev0 && ev1) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return MLA_ERR_CUDA;
+        if (cs == cudaStreamCaptureStatusActive) ev_flags = cudaEventRecordExternal;
+    }
+    if (ev0 && ev1 && cudaEventRecordWithFlags(ev0, st, ev_flags) != cudaSuccess) return MLA_ERR_CUDA;
     mla::dec::decode_bf16_kernel<<<(unsigned)(2 * G), mla::dec::THREADS, mla::dec::SMEM_ALLOC, st>>>(
         tm_c, tm_r, p);
     if (launch_status() != MLA_OK) return MLA_ERR_CUDA;
-    if (ev0 && ev1 && cudaEventRecord(ev1, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (ev0 && ev1 && cudaEventRecordWithFlags(ev1, st, ev_flags) != cudaSuccess) return MLA_ERR_CUDA;
     if (seq_lens_host &&
         !host_plan_needs_combine(seq_lens_host, B, T, HG, max_pages, p.causal, G))
         return MLA_OK;
