@@ -750,22 +750,25 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 mbar_arrive_expect_tx(XFULL(x), XT_BYTES);  // this buffer next receives tile i + 4
                 armed = i + 5;
             }
-            const float4* xp = reinterpret_cast<const float4*>(smem + OFF_X + x * XT_BYTES);
-            float s[TILE];
+            // scaled scores as packed pairs: s = (own + peer) * scale * log2(e)
+            const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(smem + OFF_X + x * XT_BYTES);
+            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
+            uint64_t s2[TILE / 2];
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k) {
-                const float4 v = xp[k * HEADS + h];
-                s[4 * k] = (__uint_as_float(own_c[4 * k]) + v.x) * p.scale_log2;
-                s[4 * k + 1] = (__uint_as_float(own_c[4 * k + 1]) + v.y) * p.scale_log2;
-                s[4 * k + 2] = (__uint_as_float(own_c[4 * k + 2]) + v.z) * p.scale_log2;
-                s[4 * k + 3] = (__uint_as_float(own_c[4 * k + 3]) + v.w) * p.scale_log2;
+                const ulonglong2 v = xp[k * HEADS + h];
+                s2[2 * k] = f2_mul(f2_add(f2_pack(__uint_as_float(own_c[4 * k]), __uint_as_float(own_c[4 * k + 1])), v.x), c2);
+                s2[2 * k + 1] =
+                    f2_mul(f2_add(f2_pack(__uint_as_float(own_c[4 * k + 2]), __uint_as_float(own_c[4 * k + 3])), v.y), c2);
+            }
+            if (c.valid < TILE) {  // only a unit's last tile has positions past the end
+#pragma unroll
+                for (int j = 0; j < TILE / 2; ++j)
+                    s2[j] = f2_pack(2 * j < c.valid ? f2_lo(s2[j]) : -INFINITY, 2 * j + 1 < c.valid ? f2_hi(s2[j]) : -INFINITY);
             }
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int j = 0; j < TILE; ++j) {
-                if (j >= c.valid) s[j] = -INFINITY;
-                mx4[j & 3] = fmaxf(mx4[j & 3], s[j]);
-            }
+            for (int j = 0; j < TILE / 2; ++j) mx4[j & 3] = fmax3(mx4[j & 3], f2_lo(s2[j]), f2_hi(s2[j]));
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
             // ---- the running maximum after the tile before (the other group)
             float m_prev = -INFINITY;
@@ -825,15 +828,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             }
             {
                 uint32_t pk[TILE / 2];
-                float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint64_t nm2 = f2_pack(-m_used, -m_used);
+                uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int j = 0; j < TILE / 2; ++j) {
-                    const float p0 = ex2(s[2 * j] - m_used);
-                    const float p1 = ex2(s[2 * j + 1] - m_used);
-                    sum4[j & 3] += p0 + p1;
+                    const uint64_t e = f2_add(s2[j], nm2);
+                    const float p0 = ex2(f2_lo(e));
+                    const float p1 = ex2(f2_hi(e));
+                    sum2[j & 1] = f2_add(sum2[j & 1], f2_pack(p0, p1));
                     pk[j] = pack_bf16x2(p0, p1);
                 }
-                l_part += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+                const uint64_t st = f2_add(sum2[0], sum2[1]);
+                l_part += f2_lo(st) + f2_hi(st);
                 tmem_st16(trow + TM_P + 16 * b, pk);
             }
             tmem_st_wait();
