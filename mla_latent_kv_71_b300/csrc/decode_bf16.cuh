@@ -91,13 +91,23 @@ constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [group][slot]
 constexpr uint32_t OFF_PUB = OFF_X + 4 * XT_BYTES;  // per-row state handed between the groups
 constexpr uint32_t PUB_BYTES = 2 * 3 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part][128]
-constexpr uint32_t OFF_BAR = OFF_PUB + PUB_BYTES;
-constexpr uint32_t NUM_BARS = 38;
+// This CTA's 32 RoPE columns of the query (128 rows x 64 B, the layout a
+// 64-byte-swizzled TMA box would have): the A operand of the RoPE part of S.
+constexpr uint32_t OFF_QPE = OFF_PUB + PUB_BYTES;      // 1 KB aligned
+constexpr uint32_t QPE_BYTES = HEADS * HALF_R * 2;
+constexpr uint32_t OFF_BAR = OFF_QPE + QPE_BYTES;
+constexpr uint32_t NUM_BARS = 35;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1 KB alignment
 
-constexpr uint32_t TM_O = 0, TM_S = 256, TM_P = 320, TM_Q = 352, TM_COLS = 512;
+// TMEM: O (128 x 256 fp32), the latent query (128 x 256 bf16), three partial
+// S buffers (tile i in i % 3, kept until its softmax has re-read it) and two
+// P buffers (tile i in i % 2): 256 + 128 + 96 + 32 = all 512 columns.
+constexpr int NS = 3;
+constexpr uint32_t TM_O = 0, TM_Q = 256, TM_S = 384, TM_P = TM_S + 32 * NS, TM_COLS = 512;
+static_assert(TM_P + 32 == TM_COLS, "TMEM map");
+static_assert(OFF_QPE % 1024 == 0, "swizzled operand alignment");
 
 // S = Q . K^T: M = 128 heads, N = 32 tokens, both operands K-major.
 constexpr uint32_t IDESC_QK = idesc_bf16(128, TILE, false, false);
@@ -320,9 +330,17 @@ struct TileIter {
     __device__ bool last_in_seg() const { return last_in_page() && lp + 1 == sg.lp1; }
     __device__ int stage() const { return (int)(page % NSTAGE); }
     __device__ uint32_t page_parity() const { return (uint32_t)((page / NSTAGE) & 1); }
-    __device__ int buf() const { return (int)(tile & 1); }
-    // parity of this tile's phase of a double-buffered barrier (n tiles back)
-    __device__ uint32_t parity(int back = 0) const { return (uint32_t)(((tile - back) >> 1) & 1); }
+    __device__ int sbuf() const { return tile % NS; }  // TMEM partial S buffer
+    // parity of the phase of an S-buffer barrier for the tile n back
+    __device__ uint32_t s_parity(int back = 0) const { return (uint32_t)(((tile - back) / NS) & 1); }
+    __device__ int buf() const { return (int)(tile & 1); }  // TMEM P buffer
+    // parity of this tile's phase of a P-buffer barrier
+    __device__ uint32_t parity() const { return (uint32_t)((tile >> 1) & 1); }
+};
+
+template <bool B>
+struct BoolC {
+    static constexpr bool value = B;
 };
 
 // What a tile group keeps of a tile between its two halves of work.
@@ -361,19 +379,21 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     auto FULL = [&](int s) { return BAR(s); };
     auto EMPTY = [&](int s) { return BAR(NSTAGE + s); };
-    auto S_FULL = [&](int b) { return BAR(8 + b); };    // S partial in TMEM (commit)
-    auto S_FREE = [&](int b) { return BAR(10 + b); };   // read by its group (4 warps)
+    // Tile i's partial S is in S buffer i % 3 (the k-th use of a buffer is
+    // phase k of its barriers), its P in P buffer i % 2.
+    auto S_FULL = [&](int k) { return BAR(8 + k); };    // partial S of the buffer's tile (commit)
+    auto S_FREE = [&](int k) { return BAR(11 + k); };   // re-read by the softmax (4 warps)
+    auto P_FULL = [&](int b) { return BAR(14 + b); };   // P in TMEM (4 warps)
+    auto PV_DONE = [&](int b) { return BAR(16 + b); };  // O += P.C of that tile (commit)
     // the peer's partial tile i lands in X[i % 2][(i / 2) % 2]: x = 2 * (i % 2) + (i / 2) % 2
-    auto XFULL = [&](int x) { return BAR(12 + x); };    // peer partial in X (1 arrive + bytes)
-    auto XFREE = [&](int x) { return BAR(16 + x); };    // peer read our copy (4 peer warps)
-    auto PV_DONE = [&](int b) { return BAR(20 + b); };  // O += P.C of that tile (commit)
-    auto M_PUB = [&](int b) { return BAR(22 + b); };    // running max after the tile (4 warps)
-    auto L_PUB = [&](int b) { return BAR(24 + b); };    // group's row sums after the tile (4 warps)
-    const uint32_t Q_FULL = BAR(26);                    // query of a unit in TMEM (4 warps)
-    const uint32_t O_FREE = BAR(27);                    // epilogue read O (4 warps)
-    const uint32_t TAIL = BAR(28);                      // partial last page landed (TMA)
-    auto DRAIN = [&](int k) { return BAR(29 + k); };    // abort: MMAs of warp 1 + k finished
-    auto P_FULL = [&](int b) { return BAR(31 + b); };   // P in TMEM (4 warps)
+    auto XFULL = [&](int x) { return BAR(18 + x); };    // peer partial in X (1 arrive + bytes)
+    auto XFREE = [&](int x) { return BAR(22 + x); };    // peer done with our copy (4 peer warps)
+    auto M_PUB = [&](int b) { return BAR(26 + b); };    // running max after the tile (4 warps)
+    auto L_PUB = [&](int b) { return BAR(28 + b); };    // group's row sums after the tile (4 warps)
+    const uint32_t Q_FULL = BAR(30);                    // query of a unit in TMEM + smem (4 warps)
+    const uint32_t O_FREE = BAR(31);                    // epilogue read O (4 warps)
+    const uint32_t TAIL = BAR(32);                      // partial last page landed (TMA)
+    auto DRAIN = [&](int k) { return BAR(33 + k); };    // abort: MMAs of warp 1 + k finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + OFF_MISC + 8);
 
@@ -382,11 +402,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             mbar_init(FULL(s), 1);
             mbar_init(EMPTY(s), 1);
         }
+        for (int k = 0; k < NS; ++k) {
+            mbar_init(S_FULL(k), 1);
+            mbar_init(S_FREE(k), 4);
+        }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(S_FULL(b), 1);
-            mbar_init(S_FREE(b), 4);
-            mbar_init(PV_DONE(b), 1);
             mbar_init(P_FULL(b), 4);
+            mbar_init(PV_DONE(b), 1);
             mbar_init(M_PUB(b), 4);
             mbar_init(L_PUB(b), 4);
         }
@@ -471,6 +493,20 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     walk.u = misc[1];
     walk.pos = misc[2];
     const bool skip = misc[3] != 0;
+    if (warp == 2 && lane == 0 && !skip) {
+        // The queries of this cluster's unit pieces, into L2 ahead of the
+        // tile groups' loads (each piece's load is on the critical path).
+        Walker w = walk;
+        Segment sg;
+        while (w.next(pv, sg)) {
+            const int bt = sg.u / p.HG;  // unit u = (b * T + t) * HG + hg
+            const int head0 = (sg.u - bt * p.HG) * HEADS;
+            const int rows = min(HEADS, p.H - head0);
+            const int64_t qrow0 = (int64_t)bt * p.H + head0;
+            bulk_prefetch_l2(p.q_lat + qrow0 * DC, (uint32_t)rows * DC * 2u);
+            bulk_prefetch_l2(p.q_pe + qrow0 * DR, (uint32_t)rows * DR * 2u);
+        }
+    }
     if (threadIdx.x == 0) {
         // Tiles of this cluster: two per page, less one for each unit piece
         // whose last page has at most TILE visible tokens.
@@ -575,10 +611,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         bool issued = false;
         const uint64_t dq0 = smem_desc(smem_u32(smem + OFF_STAGE), 16, 1024, SWZ_128B);
         const uint64_t dr0 = smem_desc(smem_u32(smem + OFF_STAGE + 4 * BOX_C_BYTES), 16, 512, SWZ_64B);
+        const uint64_t dqpe = smem_desc(smem_u32(smem + OFF_QPE), 16, 512, SWZ_64B);
         while (ok && qk.have) {
-            const int b = qk.buf();
+            const int k3 = qk.sbuf();
             if (qk.t == 0) ok = __all_sync(0xffffffffu, mbar_wait(FULL(qk.stage()), qk.page_parity(), 0x301));
-            if (ok && qk.tile >= 2) ok = __all_sync(0xffffffffu, mbar_wait(S_FREE(b), qk.parity(2), 0x302));
+            // the softmax has re-read the buffer's last tile (three back)
+            if (ok && qk.tile >= NS) ok = __all_sync(0xffffffffu, mbar_wait(S_FREE(k3), qk.s_parity(NS), 0x302));
             if (ok && qk.first_in_seg())
                 ok = __all_sync(0xffffffffu, mbar_wait(Q_FULL, (uint32_t)(qk.seg & 1), 0x303));
             if (!ok) break;
@@ -587,15 +625,15 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 const uint32_t off = (uint32_t)(qk.stage() * STAGE_BYTES);
                 const uint64_t dc = dq0 + ((uint64_t)(off + qk.t * (TILE * 128)) >> 4);
                 const uint64_t dr = dr0 + ((uint64_t)(off + qk.t * (TILE * 64)) >> 4);
-                const uint32_t d = tmem + TM_S + 32 * b;
+                const uint32_t d = tmem + TM_S + 32 * k3;
 #pragma unroll
                 for (int k = 0; k < 16; ++k)  // latent features, K-major SW128
                     mma_ts(d, tmem + TM_Q + 8 * k, dc + (uint64_t)(((k / 4) * BOX_C_BYTES + (k % 4) * 32) >> 4),
                            IDESC_QK, k > 0 ? 1u : 0u);
 #pragma unroll
-                for (int k = 0; k < 2; ++k)  // RoPE features, K-major SW64
-                    mma_ts(d, tmem + TM_Q + 128 + 8 * k, dr + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
-                tc_commit(S_FULL(b));
+                for (int k = 0; k < 2; ++k)  // RoPE features, both operands K-major SW64 in smem
+                    mma_ss(d, dqpe + (uint64_t)((k * 32) >> 4), dr + (uint64_t)((k * 32) >> 4), IDESC_QK, 1u);
+                tc_commit(S_FULL(k3));
             }
             __syncwarp();
             issued = true;
@@ -652,10 +690,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         // A group's tiles are software-pipelined: the front half of its next
         // tile (query if a unit starts there, own partial scores out of TMEM
         // and off to the peer) runs before the back half of its current one
-        // (the peer's partial in, softmax, P, epilogue), so the exchange of
-        // one tile overlaps the softmax of the one before.
+        // (own partial again from TMEM, the peer's from X, softmax, P,
+        // epilogue), so the exchange of one tile overlaps the softmax of the
+        // one before.
         const int grp = (warp - WG_WARP0) / 4;  // tiles with index % 2 == grp
-        const int b = grp;                      // their S and P buffers and barriers
+        const int b = grp;                      // their P buffers and barriers
         const int q4 = warp & 3;
         const int h = q4 * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
@@ -664,22 +703,21 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         float* pub = reinterpret_cast<float*>(smem + OFF_PUB);  // [2][3][HEADS]
         const bool leader = warp == WG_WARP0 + 4 * grp && lane == 0;
         const int my_g = (int)g_id;
-        auto xslot = [](int64_t i) { return (int)((i >> 1) & 1); };
-        auto xpar = [](int64_t i) { return (uint32_t)((i >> 2) & 1); };
+        auto xslot = [](int i) { return (i >> 1) & 1; };
+        auto xpar = [](int i) { return (uint32_t)((i >> 2) & 1); };
+        auto s_par = [](int i) { return (uint32_t)((i / NS) & 1); };  // tile i's phase of its S buffer
         bool ok = !skip;
         float m_ref = -INFINITY, l_part = 0.f;  // this group's row sum, relative to m_ref
         int64_t my_seg = -1;
         int64_t armed = misc[7 + grp], consumed = 0;
 
-        uint32_t own_c[TILE], own_n[TILE];  // partial scores of the current / next tile
-
-        // ---- front half of tile `t`; own_n receives its partial scores
-        auto front = [&](const TileIter& t) -> bool {
-            const int64_t i = t.tile;
-            if (t.first_in_seg()) {
+        // ---- front half of tile `t`
+        auto front = [&](const TileIter& t, auto may_start) -> bool {
+            const int i = t.tile;
+            if constexpr (decltype(may_start)::value) if (t.first_in_seg()) {
                 // The query of this unit replaces the last one once every
                 // score product of the tile before has completed.
-                if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(S_FULL(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x501)))
+                if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(S_FULL((i - 1) % NS), s_par(i - 1), 0x501)))
                     return false;
                 const int bt = t.sg.u / p.HG;  // unit u = (b * T + t) * HG + hg
                 const int head = (t.sg.u - bt * p.HG) * HEADS + h;
@@ -687,8 +725,17 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 const int64_t qrow = (int64_t)bt * p.H + head;
                 const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat + qrow * DC + rank * HALF_C);
                 const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * DR + rank * HALF_R);
+                {   // RoPE columns into shared memory: row h, 16-byte chunk c
+                    // at chunk c ^ ((h / 2) % 4) of its 64 bytes (64-byte swizzle)
+                    uint4 v[4];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < 4; ++c) v[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
+                    uint8_t* row = smem + OFF_QPE + h * 64;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + 16 * (c ^ ((h >> 1) & 3))) = v[c];
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {  // latent columns into TMEM
                     uint32_t r[32];
 #pragma unroll
                     for (int v = 0; v < 8; ++v) {
@@ -700,29 +747,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     }
                     tmem_st32(trow + TM_Q + 32 * c, r);
                 }
-                uint32_t r[16];
-#pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const uint4 x = live ? __ldg(qp + v) : make_uint4(0u, 0u, 0u, 0u);
-                    r[4 * v] = x.x;
-                    r[4 * v + 1] = x.y;
-                    r[4 * v + 2] = x.z;
-                    r[4 * v + 3] = x.w;
-                }
-                tmem_st16(trow + TM_Q + 128, r);
                 tmem_st_wait();
+                fence_proxy_async_smem();  // the RoPE rows, to the tensor core
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(Q_FULL);
             }
-            if (!__all_sync(0xffffffffu, mbar_wait(S_FULL(b), t.parity(), 0x502))) return false;
+            const int k3 = i % NS;
+            if (!__all_sync(0xffffffffu, mbar_wait(S_FULL(k3), s_par(i), 0x502))) return false;
             tc_fence_after();
             uint32_t r[TILE];
-            tmem_ld32(trow + TM_S + 32 * b, r);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(S_FREE(b));
-            // our copy of this group's tile four back has been read by the peer
+            tmem_ld32(trow + TM_S + 32 * k3, r);
+            // our copy of this group's tile four back is done with at the peer
             if (i >= 4 && !__all_sync(0xffffffffu, mbar_wait(XFREE(2 * grp + xslot(i)), xpar(i - 4), 0x503)))
                 return false;
             const uint32_t dst = peer_x0 + (uint32_t)xslot(i) * XT_BYTES;
@@ -730,36 +766,50 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k)
                 st_async_v4(dst + (uint32_t)(k * HEADS + h) * 16u, r[4 * k], r[4 * k + 1], r[4 * k + 2], r[4 * k + 3], pbar);
-#pragma unroll
-            for (int k = 0; k < TILE; ++k) own_n[k] = r[k];
             return true;
         };
 
-        // ---- back half of tile `c`, whose own partial scores are in own_c
-        auto back = [&](const TileInfo& c) -> bool {
-            const int64_t i = c.tile;
+        // ---- own partial scores of tile `c`, again from its buffer (the
+        // front half waited for them), taken at the start of the group's
+        // iteration: the buffer is free for tile c + 3 once all four warps
+        // have them.  The loads have completed (the wait is part of
+        // tmem_ld32) and no memory write is published, so the arrive is
+        // relaxed.
+        uint32_t own[TILE];
+        auto load_own = [&](const TileInfo& c) {
+            const int k3 = c.tile % NS;
+            tmem_ld32(trow + TM_S + 32 * k3, own);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_relaxed(S_FREE(k3));
+        };
+
+        // ---- back half of tile `c`, whose own partial scores are in `own`
+        auto back = [&](const TileInfo& c, auto may_end) -> bool {
+            const int i = c.tile;
             if (my_seg != c.seg) {  // a new unit piece: this group's sums restart
                 my_seg = c.seg;
                 m_ref = -INFINITY;
                 l_part = 0.f;
             }
             const int x = 2 * grp + xslot(i);
-            if (!__all_sync(0xffffffffu, mbar_wait<true>(XFULL(x), xpar(i), 0x504))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(XFULL(x), xpar(i), 0x504))) return false;
             consumed = i + 1;
             if (leader && i + 4 < n_tiles) {
                 mbar_arrive_expect_tx(XFULL(x), XT_BYTES);  // this buffer next receives tile i + 4
                 armed = i + 5;
             }
+            uint8_t* xbuf = smem + OFF_X + x * XT_BYTES;
             // scaled scores as packed pairs: s = (own + peer) * scale * log2(e)
-            const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(smem + OFF_X + x * XT_BYTES);
+            const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xbuf);
             const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
             uint64_t s2[TILE / 2];
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k) {
                 const ulonglong2 v = xp[k * HEADS + h];
-                s2[2 * k] = f2_mul(f2_add(f2_pack(__uint_as_float(own_c[4 * k]), __uint_as_float(own_c[4 * k + 1])), v.x), c2);
+                s2[2 * k] = f2_mul(f2_add(f2_pack(__uint_as_float(own[4 * k]), __uint_as_float(own[4 * k + 1])), v.x), c2);
                 s2[2 * k + 1] =
-                    f2_mul(f2_add(f2_pack(__uint_as_float(own_c[4 * k + 2]), __uint_as_float(own_c[4 * k + 3])), v.y), c2);
+                    f2_mul(f2_add(f2_pack(__uint_as_float(own[4 * k + 2]), __uint_as_float(own[4 * k + 3])), v.y), c2);
             }
             if (c.valid < TILE) {  // only a unit's last tile has positions past the end
 #pragma unroll
@@ -794,10 +844,16 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 need = mx > m_prev + RESCALE_THRESHOLD;
                 m_used = need ? mx : m_prev;
             }
+            bool p_free = i < 2;
             if (__any_sync(0xffffffffu, need)) {
                 // O moves to the new maximum once the tile before has been
                 // added to it (and with it every earlier one: the products
-                // land in tile order), and before any later tile is
+                // land in tile order), and before any later tile is.  The
+                // product two back is waited for first: then the other
+                // parity's barrier has only the tile before outstanding.
+                if (!p_free && !__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)(((i - 2) >> 1) & 1), 0x508)))
+                    return false;
+                p_free = true;
                 if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x507)))
                     return false;
                 tc_fence_after();
@@ -821,7 +877,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 m_ref = m_used;
             }
             // ---- P[b] is free once the tile two back has been multiplied
-            if (i >= 2) {
+            if (!p_free) {
                 if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)(((i - 2) >> 1) & 1), 0x508)))
                     return false;
                 tc_fence_after();
@@ -847,51 +903,76 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             pub[(b * 3 + 1) * HEADS + h] = m_ref;
             pub[(b * 3 + 2) * HEADS + h] = l_part;
             __syncwarp();
+            bool x_held = false;  // X buffer kept as the epilogue's staging area
+            if constexpr (decltype(may_end)::value) x_held = c.last;
             if (lane == 0) {
                 mbar_arrive(P_FULL(b));
                 mbar_arrive(L_PUB(b));
                 // Every value read from this X buffer has gone into P, now stored.
-                mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));
+                if (!x_held) mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));
             }
-            if (c.last) {
-                // ---- epilogue: O / l of this CTA's 256 columns, lse
+            if constexpr (decltype(may_end)::value) if (c.last) {
+                // ---- epilogue: O / l of this CTA's 256 columns, lse.  O is
+                // complete once this tile's product is (the products land in
+                // tile order).
                 if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)((i >> 1) & 1), 0x509))) return false;
                 tc_fence_after();
                 const float l = l_part + (c.first ? 0.f : l_oth * ex2(m_oth - m_used));
                 const int bt = c.u / p.HG;  // unit u = (b * T + t) * HG + hg
-                const int head = (c.u - bt * p.HG) * HEADS + h;
-                const bool live = head < p.H;
-                const int64_t qrow = (int64_t)bt * p.H + head;
+                const int head0 = (c.u - bt * p.HG) * HEADS + q4 * 32;  // head of this warp's row 0
+                const int64_t qrow0 = (int64_t)bt * p.H + head0;
                 const float inv_l = 1.f / l;
+                // Rows go out through this tile's X buffer (the 4 KB this warp
+                // read): each thread puts its row's 16-byte chunks in, then the
+                // warp stores whole 64- or 128-byte row pieces per instruction
+                // instead of 32 scattered 16-byte ones.  Chunk j of row r sits
+                // in slot (r + j) % 8 of its 8-slot group, which keeps both
+                // passes free of bank conflicts.
+                auto stg = [&](int r, int j) -> uint4* {
+                    return reinterpret_cast<uint4*>(xbuf + j * (HEADS * 16) + q4 * 512 + 16 * ((r & 24) | ((r + j) & 7)));
+                };
                 if (c.slot < 0) {
-                    __nv_bfloat16* dst = p.o + qrow * DC + rank * HALF_C;
+                    __nv_bfloat16* dst = p.o + qrow0 * DC + rank * HALF_C + 8 * (lane & 3);
 #pragma unroll 1
                     for (int cc = 0; cc < HALF_C; cc += 32) {
                         uint32_t r[32];
                         tmem_ld32(trow + TM_O + cc, r);
-                        if (live) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + cc);
 #pragma unroll
-                            for (int v = 0; v < 4; ++v)
-                                d4[v] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(r[8 * v]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l),
-                                    pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l),
-                                    pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l),
-                                    pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l));
+                        for (int v = 0; v < 4; ++v)
+                            *stg(lane, v) = make_uint4(
+                                pack_bf16x2(__uint_as_float(r[8 * v]) * inv_l, __uint_as_float(r[8 * v + 1]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv_l, __uint_as_float(r[8 * v + 3]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l));
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {  // 8 rows x 64 bytes per store
+                            const int row = 8 * k + (lane >> 2);
+                            if (head0 + row < p.H)
+                                *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 3);
                         }
+                        __syncwarp();
                     }
-                    if (live && rank == 0) p.lse[qrow] = (m_used + __log2f(l)) * LN2;
+                    if (head0 + lane < p.H && rank == 0) p.lse[qrow0 + lane] = (m_used + __log2f(l)) * LN2;
                 } else {
-                    float* dst = p.ws_o + (c.slot * HEADS + h) * DC + rank * HALF_C;
+                    float* dst = p.ws_o + (int64_t)(c.slot * HEADS + q4 * 32) * DC + rank * HALF_C + 4 * (lane & 7);
 #pragma unroll 1
                     for (int cc = 0; cc < HALF_C; cc += 32) {
                         uint32_t r[32];
                         tmem_ld32(trow + TM_O + cc, r);
-                        float4* d4 = reinterpret_cast<float4*>(dst + cc);
 #pragma unroll
                         for (int v = 0; v < 8; ++v)
-                            d4[v] = make_float4(__uint_as_float(r[4 * v]) * inv_l, __uint_as_float(r[4 * v + 1]) * inv_l,
-                                                __uint_as_float(r[4 * v + 2]) * inv_l, __uint_as_float(r[4 * v + 3]) * inv_l);
+                            *stg(lane, v) = make_uint4(__float_as_uint(__uint_as_float(r[4 * v]) * inv_l),
+                                                       __float_as_uint(__uint_as_float(r[4 * v + 1]) * inv_l),
+                                                       __float_as_uint(__uint_as_float(r[4 * v + 2]) * inv_l),
+                                                       __float_as_uint(__uint_as_float(r[4 * v + 3]) * inv_l));
+                        __syncwarp();
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {  // 4 rows x 128 bytes per store
+                            const int row = 4 * k + (lane >> 3);
+                            *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 7);
+                        }
+                        __syncwarp();
                     }
                     if (rank == 0) p.ws_lse[c.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
                 }
@@ -899,7 +980,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     p.ws_unit[c.u] = make_int2((int)c.g_first, c.g_last);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(O_FREE);
+                if (lane == 0) {
+                    mbar_arrive(O_FREE);
+                    mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));  // staging done
+                }
             }
             return true;
         };
@@ -910,26 +994,34 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         TileInfo cur;
         bool have_cur = false;
         if (ok && it.have) {
-            ok = front(it);
-#pragma unroll
-            for (int k = 0; k < TILE; ++k) own_c[k] = own_n[k];
+            ok = front(it, BoolC<true>{});
             cur.set(it);
             have_cur = true;
             it.advance(pv);
             if (it.have) it.advance(pv);
         }
-        // `it` now points at the group's next tile: its front half runs
-        // before the back half of `cur`.
+        // `it` now points at the group's next tile.  Within a unit piece its
+        // front half runs before the back half of `cur`, so the exchange of
+        // one tile overlaps the softmax of the one before.  Where the piece
+        // changes the back half goes first: the front half of a piece's first
+        // tile loads the query and everything after it waits for that query's
+        // scores, so the old piece's epilogue then overlaps the query load
+        // instead of following it.  (A piece's last tile is always followed
+        // by another piece or by nothing, so only that order needs the
+        // epilogue, and only it the query load.)
         while (ok && have_cur) {
-            if (it.have) {
-                ok = front(it);
+            load_own(cur);
+            if (!it.have || it.seg != cur.seg) {
+                ok = back(cur, BoolC<true>{});
+                if (!ok || !it.have) break;
+                ok = front(it, BoolC<true>{});
+            } else {  // same piece: `it` does not start one
+                ok = front(it, BoolC<false>{});
                 if (!ok) break;
+                ok = back(cur, BoolC<false>{});
             }
-            ok = back(cur);
-            if (!ok || !it.have) break;
+            if (!ok) break;
             cur.set(it);
-#pragma unroll
-            for (int k = 0; k < TILE; ++k) own_c[k] = own_n[k];
             it.advance(pv);
             if (it.have) it.advance(pv);
         }

@@ -55,6 +55,13 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Arrive without release semantics: for signals that publish no memory
+// writes of this thread (a default arrive also waits for this thread's
+// earlier stores, remote ones included, to complete).
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
@@ -106,18 +113,23 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity.  `where` is recorded in
-// the status word's detail field when the wait gives up.
+// the status word's detail field when the wait gives up.  The status word
+// (another CTA gave up) and the clock are only looked at every 16th retry:
+// the status word is a global load, and a phase that completes while the
+// thread waits for it is only seen after it returns.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t where) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    while (true) {
+    for (uint32_t n = 1;; ++n) {
         if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
             return true;
-        if (device_status_raised()) return false;
-        if (global_timer_ns() - t0 > MLA_WAIT_LIMIT_NS) {
-            raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
-            return false;
+        if ((n & 15u) == 0u) {
+            if (device_status_raised()) return false;
+            if (global_timer_ns() - t0 > MLA_WAIT_LIMIT_NS) {
+                raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
+                return false;
+            }
         }
     }
 }
@@ -143,6 +155,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// Bring `bytes` (a multiple of 16) of global memory at a 16-byte aligned
+// address into L2, asynchronously.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
