@@ -1048,13 +1048,17 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 }
 
 // Merge the partial results of units cut between clusters.  One warp per
-// head row (8 rows per 256-thread block): lane k < pieces reads piece k's
-// lse, the warp forms the log-sum-exp weights with shuffles, and each lane
-// then merges 16 of the row's 512 columns from every piece.  Also writes
-// o = 0, lse = -inf for units that see no cached position.
-constexpr int COMBINE_ROWS = 8;
+// head row (4 rows per 128-thread block, at most 64 registers, so that 8 blocks fit
+// an SM).  Once the unit's piece range is known, the loads the merge needs are
+// issued together: lane k < pieces reads piece k's lse, and each lane reads
+// its 16 of the row's 512 columns from the first two pieces (further pieces
+// take a loop).  The warp forms the
+// log-sum-exp weights with shuffles.  Also writes o = 0, lse = -inf for
+// units that see no cached position.
+constexpr int COMBINE_ROWS = 4;
+constexpr int COMBINE_UNROLL = 2;
 
-__global__ void __launch_bounds__(32 * COMBINE_ROWS)
+__global__ void __launch_bounds__(32 * COMBINE_ROWS, 8)
 decode_combine_kernel(const Params p) {
     if (device_status_raised()) return;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -1077,34 +1081,50 @@ decode_combine_kernel(const Params p) {
     }
     if (gg.x == gg.y) return;  // written directly by the attention kernel
     const int n = gg.y - gg.x + 1;
-    float m = -INFINITY;
-    for (int k = lane; k < n; k += 32) m = fmaxf(m, p.ws_lse[(int64_t)(gg.x + k + u) * HEADS + h]);
+    const int64_t r0 = (int64_t)(gg.x + u) * HEADS + h;  // piece k's row: r0 + k * HEADS
+    const float lse_l = lane < n ? p.ws_lse[r0 + (int64_t)lane * HEADS] : -INFINITY;
+    float4 x[COMBINE_UNROLL][4];
+#pragma unroll
+    for (int k = 0; k < COMBINE_UNROLL; ++k) {
+        const float4* src = reinterpret_cast<const float4*>(p.ws_o + (r0 + (int64_t)k * HEADS) * DC + 16 * lane);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) x[k][v] = k < n ? __ldcg(src + v) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float m = lse_l;
+    for (int k = lane + 32; k < n; k += 32) m = fmaxf(m, p.ws_lse[r0 + (int64_t)k * HEADS]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    float sum = 0.f;
-    for (int k = lane; k < n; k += 32) sum += __expf(p.ws_lse[(int64_t)(gg.x + k + u) * HEADS + h] - m);
+    float sum = __expf(lse_l - m);
+    for (int k = lane + 32; k < n; k += 32) sum += __expf(p.ws_lse[r0 + (int64_t)k * HEADS] - m);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float L = m + __logf(sum);
+    const float w_l = __expf(lse_l - L);  // piece `lane`'s weight (0 past the last piece)
     float acc[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-    for (int k0 = 0; k0 < n; k0 += 32) {
-        const int kk = k0 + lane;
-        const float w_l = kk < n ? __expf(p.ws_lse[(int64_t)(gg.x + kk + u) * HEADS + h] - L) : 0.f;
-        const int cnt = n - k0 < 32 ? n - k0 : 32;
-        for (int k = 0; k < cnt; ++k) {
-            const float w = __shfl_sync(0xffffffffu, w_l, k);
-            const float4* src = reinterpret_cast<const float4*>(
-                p.ws_o + ((int64_t)(gg.x + k0 + k + u) * HEADS + h) * DC + 16 * lane);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const float4 x = __ldcg(src + v);
-                acc[4 * v] = fmaf(w, x.x, acc[4 * v]);
-                acc[4 * v + 1] = fmaf(w, x.y, acc[4 * v + 1]);
-                acc[4 * v + 2] = fmaf(w, x.z, acc[4 * v + 2]);
-                acc[4 * v + 3] = fmaf(w, x.w, acc[4 * v + 3]);
-            }
+    for (int k = 0; k < COMBINE_UNROLL; ++k) {
+        const float w = __shfl_sync(0xffffffffu, w_l, k);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            acc[4 * v] = fmaf(w, x[k][v].x, acc[4 * v]);
+            acc[4 * v + 1] = fmaf(w, x[k][v].y, acc[4 * v + 1]);
+            acc[4 * v + 2] = fmaf(w, x[k][v].z, acc[4 * v + 2]);
+            acc[4 * v + 3] = fmaf(w, x[k][v].w, acc[4 * v + 3]);
+        }
+    }
+    for (int k = COMBINE_UNROLL; k < n; ++k) {  // long runs of pieces
+        const float wk = k < 32 ? __shfl_sync(0xffffffffu, w_l, k)
+                                : __expf(p.ws_lse[r0 + (int64_t)k * HEADS] - L);
+        const float4* src = reinterpret_cast<const float4*>(p.ws_o + (r0 + (int64_t)k * HEADS) * DC + 16 * lane);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const float4 y = __ldcg(src + v);
+            acc[4 * v] = fmaf(wk, y.x, acc[4 * v]);
+            acc[4 * v + 1] = fmaf(wk, y.y, acc[4 * v + 1]);
+            acc[4 * v + 2] = fmaf(wk, y.z, acc[4 * v + 2]);
+            acc[4 * v + 3] = fmaf(wk, y.w, acc[4 * v + 3]);
         }
     }
     reinterpret_cast<uint4*>(dst)[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
