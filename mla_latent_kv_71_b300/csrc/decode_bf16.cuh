@@ -143,20 +143,39 @@ struct Params {
 // kernel (every CTA derives it independently) and by the host
 // (mla_decode_plan, and the decision to skip the combine launch).
 //
-// Units u = ((b*T + t)*HG + hg) are laid end to end by their pages; the line
-// of `total` pages is cut into G = min(clusters, total) contiguous ranges,
-// range g = [total*g/G, total*(g+1)/G), none of them empty.  A unit cut by a
-// range boundary is processed in pieces; piece (g, u) writes partial slot
-// g + u, which is unique because both g and u only grow along the line.
+// Units u = ((b*T + t)*HG + hg) are laid end to end by their pages on a
+// virtual line where each non-empty unit after the first is preceded by C
+// virtual pages: starting a unit piece (the last piece's epilogue, the next
+// query) costs a cluster about as much as C pages of attention, so a range
+// that holds a unit boundary should get fewer real pages.  C is
+// BOUNDARY_PAGES on lines of at least 8 pages per cluster and 0 otherwise.
+// The line of V virtual positions is cut into G = min(clusters, total real
+// pages) contiguous ranges, range g = [V*g/G, V*(g+1)/G), none of them
+// without a real page (a range spans at least 8 positions when C > 0).  A
+// unit cut by a range boundary is processed in pieces; piece (g, u) writes
+// partial slot g + u, which is unique because both g and u only grow along
+// the line.
 
 struct PlanView {
     const int32_t* seq_lens;  // [B]
     int B, T, HG, max_pages, causal;
 };
 
-// Plan quantities (units, pages of the line, clusters, slots, tiles) are
-// 32-bit: the host rejects shapes where B*T*HG*max_pages or max_pages*64
-// reach 2^31, which bounds all of them.
+// Plan quantities (units, positions of the line, clusters, slots, tiles) are
+// 32-bit: the host rejects shapes where B*T*HG*(max_pages + BOUNDARY_PAGES)
+// or max_pages*64 reach 2^31, which bounds all of them.
+
+constexpr int BOUNDARY_PAGES = 3;
+
+// Virtual pages before each non-empty unit after the first.
+__host__ __device__ __forceinline__ int boundary_pages(int total, int launched) {
+    return total >= 8 * launched ? BOUNDARY_PAGES : 0;
+}
+
+// Length of the virtual line of `total` real pages in `units` non-empty units.
+__host__ __device__ __forceinline__ int virtual_total(int total, int units, int C) {
+    return units > 0 ? total + C * (units - 1) : 0;
+}
 
 // Visible positions and pages of unit u.
 struct Unit {
@@ -191,7 +210,7 @@ __host__ __device__ __forceinline__ int clusters_used(int total, int launched) {
     return total < launched ? total : launched;
 }
 
-// The range (cluster) holding page x of the line.
+// The range (cluster) holding position x of the line.
 __host__ __device__ __forceinline__ int cluster_of_page(int x, int total, int G) {
     int g = (int)((int64_t)x * G / total);
     while (g + 1 < G && range_start(total, g + 1, G) <= x) ++g;
@@ -208,24 +227,26 @@ struct Segment {
     int g_first, g_last;   // clusters holding the unit's first and last page
 };
 
-// Walks the units overlapping cluster g's range, in line order.
+// Walks the units overlapping cluster g's range, in line order (positions
+// rs, re, total and pos are on the virtual line).
 struct Walker {
-    int U, rs, re, total, G, g;
-    int u, pos;  // next unit and its first page on the line
+    int U, rs, re, total, G, g, C;
+    int u, pos;  // next unit and the position of its first page
     __host__ __device__ bool next(const PlanView& v, Segment& s) {
         if (rs >= re) return false;  // an empty range has no piece
         while (pos < re && u < U) {
             const Unit un = unit_of(v, u);
-            const int start = pos;
-            pos += un.pages;
             const int cu = u++;
-            if (un.pages == 0 || pos <= rs) continue;
+            if (un.pages == 0) continue;
+            const int start = pos, end = pos + un.pages;
+            pos = end + C;
+            if (end <= rs) continue;
             s.u = cu;
             s.len = un.len;
             s.lp0 = (rs > start ? rs : start) - start;
-            s.lp1 = (re < pos ? re : pos) - start;
+            s.lp1 = (re < end ? re : end) - start;
             s.g_first = cluster_of_page(start, total, G);
-            s.g_last = cluster_of_page(pos - 1, total, G);
+            s.g_last = cluster_of_page(end - 1, total, G);
             s.slot = (s.g_first == s.g_last) ? -1 : g + cu;
             return true;
         }
@@ -237,33 +258,39 @@ struct Walker {
 inline Walker host_walker(const PlanView& v, int launched, int g) {
     Walker w;
     w.U = v.B * v.T * v.HG;
-    int total = 0;
-    for (int u = 0; u < w.U; ++u) total += unit_of(v, u).pages;
-    w.total = total;
+    int total = 0, units = 0;
+    for (int u = 0; u < w.U; ++u) {
+        const int n = unit_of(v, u).pages;
+        total += n;
+        units += n > 0;
+    }
+    w.C = boundary_pages(total, launched);
+    w.total = virtual_total(total, units, w.C);
     w.G = clusters_used(total, launched);
     w.g = g;
     w.rs = w.re = 0;
     w.u = w.U;
     w.pos = 0;
     if (total == 0 || g >= w.G) return w;
-    w.rs = range_start(total, g, w.G);
-    w.re = range_start(total, g + 1, w.G);
+    w.rs = range_start(w.total, g, w.G);
+    w.re = range_start(w.total, g + 1, w.G);
     int pos = 0;
     for (int u = 0; u < w.U; ++u) {
         const int n = unit_of(v, u).pages;
+        if (n == 0) continue;
         if (w.rs < pos + n) {
             w.u = u;
             w.pos = pos;
             break;
         }
-        pos += n;
+        pos += n + w.C;
     }
     return w;
 }
 
 // Host-side bound check for the 32-bit plan arithmetic.
 inline bool plan_fits_int32(int B, int T, int HG, int max_pages) {
-    return (int64_t)B * T * HG * max_pages < ((int64_t)1 << 31) &&
+    return (int64_t)B * T * HG * (max_pages + BOUNDARY_PAGES) < ((int64_t)1 << 31) &&
            (int64_t)max_pages * PAGE < ((int64_t)1 << 31);
 }
 
@@ -440,53 +467,81 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     const int64_t U = (int64_t)p.B * p.T * p.HG;
     const int64_t launched = num_clusters_x(), g_id = cluster_id_x();
     if (warp == 0) {
-        // Warp 0 sums the pages of contiguous chunks of units and scans them
-        // with shuffles; the lane holding the range start finds its unit.
+        // Warp 0 sums the pages (and counts the non-empty units) of
+        // contiguous chunks of units and scans them with shuffles; then each
+        // lane walks its units again on the virtual line, the first unit that
+        // reaches into the range is recorded, and all lanes count the range's
+        // tiles: two per page, less one for each unit whose last page lies in
+        // the range with at most TILE visible tokens.
         const int64_t chunk = (U + 31) / 32;
         const int64_t u0 = min(U, (int64_t)lane * chunk), u1 = min(U, u0 + chunk);
-        int64_t sum = 0;
+        int64_t sum = 0, cnt = 0;
         bool bad = false;
         for (int64_t u = u0; u < u1; ++u) {
             const Unit un = unit_of(pv, u);
             sum += un.pages;
+            cnt += un.pages > 0;
             bad |= un.bad_len;
         }
         if (bad && rank == 0 && g_id == 0) raise_device_status(MLA_DEV_BOUNDS, 0x10);
-        int64_t incl = sum;
+        int64_t incl = sum, incl_cnt = cnt;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int64_t vc = __shfl_up_sync(0xffffffffu, incl_cnt, o);
+            if (lane >= o) {
+                incl += v;
+                incl_cnt += vc;
+            }
         }
         const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-        const int64_t pre = incl - sum;
+        const int64_t units = __shfl_sync(0xffffffffu, incl_cnt, 31);
+        const int C = boundary_pages((int)total, (int)launched);
+        const int64_t V = virtual_total((int)total, (int)units, C);
         if (lane == 0) {
-            misc[0] = total;  // total pages
+            misc[0] = V;      // virtual positions of the line
             misc[1] = U;      // first unit of this cluster's range (default: none)
             misc[2] = 0;
             misc[3] = device_status_raised() ? 1 : 0;  // one decision for the whole CTA
+            misc[4] = C;
+            misc[5] = total;  // real pages
         }
         __syncwarp();
         const int64_t G = clusters_used(total, launched);
-        const int64_t rs = g_id < G ? range_start(total, g_id, G) : total;
-        if (g_id < G && rs >= pre && rs < pre + sum) {
-            int64_t pos = pre;
-            for (int64_t u = u0; u < u1; ++u) {
-                const int64_t n = unit_of(pv, u).pages;
-                if (rs < pos + n) {
-                    misc[1] = u;
-                    misc[2] = pos;
-                    break;
+        const int64_t rs = g_id < G ? range_start(V, g_id, G) : V;
+        const int64_t re = g_id < G ? range_start(V, g_id + 1, G) : V;
+        int64_t tiles = 0, first_u = -1, first_pos = 0;
+        int64_t pos = (incl - sum) + C * (incl_cnt - cnt);  // the chunk's first non-empty unit
+        if (rs < re) {
+            for (int64_t u = u0; u < u1 && pos < re; ++u) {
+                const Unit un = unit_of(pv, u);
+                if (un.pages == 0) continue;
+                const int64_t s0 = pos, s1 = pos + un.pages;
+                pos = s1 + C;
+                if (s1 <= rs) continue;
+                if (first_u < 0) {
+                    first_u = u;
+                    first_pos = s0;
                 }
-                pos += n;
+                tiles += 2 * (min(s1, re) - max(s0, rs));
+                if (s1 <= re && un.len - (un.pages - 1) * PAGE <= TILE) tiles -= 1;
             }
         }
+        const uint32_t found = __ballot_sync(0xffffffffu, first_u >= 0);
+        if (found != 0u && lane == __ffs(found) - 1) {  // the lowest lane's is the range's first
+            misc[1] = first_u;
+            misc[2] = first_pos;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, o);
+        if (lane == 0) misc[6] = misc[3] ? 0 : tiles;
     }
     __syncthreads();  // misc[1], misc[2] (the range's first unit) are written above
     Walker walk;
     walk.U = U;
     walk.total = misc[0];
-    walk.G = clusters_used(walk.total, launched);
+    walk.C = (int)misc[4];
+    walk.G = clusters_used(misc[5], launched);
     walk.g = g_id;
     walk.rs = g_id < walk.G ? range_start(walk.total, g_id, walk.G) : 0;
     walk.re = g_id < walk.G ? range_start(walk.total, g_id + 1, walk.G) : 0;
@@ -508,17 +563,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         }
     }
     if (threadIdx.x == 0) {
-        // Tiles of this cluster: two per page, less one for each unit piece
-        // whose last page has at most TILE visible tokens.
-        Walker w = walk;
-        Segment sg;
-        int64_t n = 0;
-        while (!skip && w.next(pv, sg)) n += 2 * (sg.lp1 - sg.lp0) - (page_valid(sg, sg.lp1 - 1) > TILE ? 0 : 1);
         // The peer's partial tiles 0..3 land in the four X buffers; later
         // tiles are armed by the groups as they consume these.
+        const int64_t n = misc[6];
         for (int64_t i = 0; i < n && i < 4; ++i)
             mbar_arrive_expect_tx(XFULL((int)(2 * (i & 1) + ((i >> 1) & 1))), XT_BYTES);
-        misc[6] = n;
         for (int g = 0; g < 2; ++g) {
             misc[7 + g] = n < 4 ? n : 4;  // group g: tiles below this were armed
             misc[9 + g] = 0;              // ... and its tiles below this consumed
@@ -527,7 +576,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    cluster_sync();  // the peer's barriers are initialised (and armed) before any remote access
+    // The peer's barriers are initialised before any remote access (their
+    // arming needs no order: transaction bytes may land before it).
+    cluster_sync_relaxed();
     const uint32_t tmem = *tmem_slot;
     const int64_t n_tiles = misc[6];
 
@@ -735,17 +786,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + 16 * (c ^ ((h >> 1) & 3))) = v[c];
                 }
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {  // latent columns into TMEM
-                    uint32_t r[32];
+                for (int half = 0; half < 2; ++half) {  // latent columns into TMEM, 128 at a time
+                    uint32_t r[64];
 #pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        const uint4 x = live ? __ldg(ql + c * 8 + v) : make_uint4(0u, 0u, 0u, 0u);
+                    for (int v = 0; v < 16; ++v) {
+                        const uint4 x = live ? __ldg(ql + 16 * half + v) : make_uint4(0u, 0u, 0u, 0u);
                         r[4 * v] = x.x;
                         r[4 * v + 1] = x.y;
                         r[4 * v + 2] = x.z;
                         r[4 * v + 3] = x.w;
                     }
-                    tmem_st32(trow + TM_Q + 32 * c, r);
+                    tmem_st32(trow + TM_Q + 64 * half, *reinterpret_cast<const uint32_t(*)[32]>(r));
+                    tmem_st32(trow + TM_Q + 64 * half + 32, *reinterpret_cast<const uint32_t(*)[32]>(r + 32));
                 }
                 tmem_st_wait();
                 fence_proxy_async_smem();  // the RoPE rows, to the tensor core

@@ -138,13 +138,15 @@ bool host_plan_needs_combine(const int32_t* lens, int B, int T, int HG, int max_
         if (un.pages == 0 || un.bad_len) return true;
         total += un.pages;
     }
+    const int C = mla::dec::boundary_pages(total, launched);
+    const int V = mla::dec::virtual_total(total, U, C);
     const int G = mla::dec::clusters_used(total, launched);
     int pos = 0;
     for (int u = 0; u < U; ++u) {
         const int n = mla::dec::unit_of(v, u).pages;
-        if (mla::dec::cluster_of_page(pos, total, G) != mla::dec::cluster_of_page(pos + n - 1, total, G))
+        if (mla::dec::cluster_of_page(pos, V, G) != mla::dec::cluster_of_page(pos + n - 1, V, G))
             return true;
-        pos += n;
+        pos += n + C;
     }
     return false;
 }

@@ -212,6 +212,15 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
     return r;
 }
 
+// Cluster barrier whose arrive orders nothing: for the start of a kernel,
+// after fence.mbarrier_init has published this CTA's barriers to the
+// cluster (a release arrive costs about a microsecond here).
+__device__ __forceinline__ void cluster_sync_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.aligned;" ::
+                     : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::

@@ -51,13 +51,29 @@ def check_plan(lens, T, H, max_pages, causal, clusters):
         if n:
             cl = sorted(p["cluster"] for p in by_unit[u])
             assert cl == list(range(by_unit[u][0]["g_first"], by_unit[u][0]["g_last"] + 1))
-    # ranges are balanced: no cluster holds more than ceil(total / G) pages
+    # Ranges are equal cuts of the virtual line, on which each non-empty unit
+    # after the first is preceded by C virtual pages (C = 3 on lines of at
+    # least 8 pages per cluster, else 0): no cluster holds more than
+    # ceil(V / G) real pages, every cluster holds some, and clusters whose
+    # range holds a unit boundary hold fewer real pages on average than those
+    # without (a range that starts or ends inside a gap holds fewer too).
+    nonempty = sum(1 for n in pages if n)
+    C = 3 if total >= 8 * clusters else 0
+    V = total + C * (nonempty - 1) if nonempty else 0
     per = {}
     for p in pieces:
         per[p["cluster"]] = per.get(p["cluster"], 0) + p["lp1"] - p["lp0"]
     if total:
-        assert max(per.values()) <= math.ceil(total / G)
+        assert max(per.values()) <= math.ceil(V / G)
         assert len(per) == G
+        if C:
+            npieces = {}
+            for p in pieces:
+                npieces[p["cluster"]] = npieces.get(p["cluster"], 0) + 1
+            one = [per[g] for g in per if npieces[g] == 1]
+            more = [per[g] for g in per if npieces[g] > 1]
+            if one and more:
+                assert sum(more) / len(more) < sum(one) / len(one)
     return pieces
 
 
