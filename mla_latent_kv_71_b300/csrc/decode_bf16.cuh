@@ -852,16 +852,16 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 armed = i + 5;
             }
             uint8_t* xbuf = smem + OFF_X + x * XT_BYTES;
-            // scaled scores as packed pairs: s = (own + peer) * scale * log2(e)
+            // unscaled scores as packed pairs: own + peer partial (the scale
+            // scale * log2(e) > 0 is applied to the maximum here and inside
+            // the exponent's fused multiply-add below)
             const ulonglong2* xp = reinterpret_cast<const ulonglong2*>(xbuf);
-            const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
             uint64_t s2[TILE / 2];
 #pragma unroll
             for (int k = 0; k < TILE / 4; ++k) {
                 const ulonglong2 v = xp[k * HEADS + h];
-                s2[2 * k] = f2_mul(f2_add(f2_pack(__uint_as_float(own[4 * k]), __uint_as_float(own[4 * k + 1])), v.x), c2);
-                s2[2 * k + 1] =
-                    f2_mul(f2_add(f2_pack(__uint_as_float(own[4 * k + 2]), __uint_as_float(own[4 * k + 3])), v.y), c2);
+                s2[2 * k] = f2_add(f2_pack(__uint_as_float(own[4 * k]), __uint_as_float(own[4 * k + 1])), v.x);
+                s2[2 * k + 1] = f2_add(f2_pack(__uint_as_float(own[4 * k + 2]), __uint_as_float(own[4 * k + 3])), v.y);
             }
             if (c.valid < TILE) {  // only a unit's last tile has positions past the end
 #pragma unroll
@@ -871,7 +871,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int j = 0; j < TILE / 2; ++j) mx4[j & 3] = fmax3(mx4[j & 3], f2_lo(s2[j]), f2_hi(s2[j]));
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
             // ---- the running maximum after the tile before (the other group)
             float m_prev = -INFINITY;
             if (i >= 1) {
@@ -937,10 +937,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             {
                 uint32_t pk[TILE / 2];
                 const uint64_t nm2 = f2_pack(-m_used, -m_used);
+                const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
                 uint64_t sum2[2] = {0ull, 0ull};
 #pragma unroll
                 for (int j = 0; j < TILE / 2; ++j) {
-                    const uint64_t e = f2_add(s2[j], nm2);
+                    const uint64_t e = f2_fma(s2[j], c2, nm2);  // s * scale * log2(e) - m
                     const float p0 = ex2(f2_lo(e));
                     const float p1 = ex2(f2_hi(e));
                     sum2[j & 1] = f2_add(sum2[j & 1], f2_pack(p0, p1));
