@@ -872,6 +872,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 #pragma unroll
             for (int j = 0; j < TILE / 2; ++j) mx4[j & 3] = fmax3(mx4[j & 3], f2_lo(s2[j]), f2_hi(s2[j]));
             const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * p.scale_log2;
+            // Every value read from this X buffer is in registers: it goes back
+            // to the peer now -- except at a piece's end, where the epilogue
+            // stages its rows there first (the last tile always takes the
+            // epilogue-compiled path).
+            __syncwarp();
+            if (!c.last && lane == 0) mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));
             // ---- the running maximum after the tile before (the other group)
             float m_prev = -INFINITY;
             if (i >= 1) {
@@ -956,13 +962,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             pub[(b * 3 + 1) * HEADS + h] = m_ref;
             pub[(b * 3 + 2) * HEADS + h] = l_part;
             __syncwarp();
-            bool x_held = false;  // X buffer kept as the epilogue's staging area
-            if constexpr (decltype(may_end)::value) x_held = c.last;
             if (lane == 0) {
                 mbar_arrive(P_FULL(b));
                 mbar_arrive(L_PUB(b));
-                // Every value read from this X buffer has gone into P, now stored.
-                if (!x_held) mbar_arrive_remote_relaxed(map_to_rank(XFREE(x), peer));
             }
             if constexpr (decltype(may_end)::value) if (c.last) {
                 // ---- epilogue: O / l of this CTA's 256 columns, lse.  O is
