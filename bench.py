@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
+    python bench.py --projections   (rows a1/a8: absorb_q and out_proj alone)
 
 A step is one decode step of the hot path over one synthetic batch: the
 paged absorbed attention kernel and, when the batch is cut across SMs, its
@@ -460,6 +461,67 @@ def run_reference(args, rank, world):
     }
 
 
+def run_projections(args, local):
+    """The query absorption (q_lat = W^UK^T q_nope) and the output projection
+    (out = W^O concat_i W^UV_i o_i) at the two-token workload's sizes (64
+    query rows x 128 heads, d_h 128, d_c 512, d 7168), each timed alone: CUDA
+    events around single launches, L2 flushed (a 256 MB write) before each,
+    median over the timed launches.  Both are bound by their weight bytes
+    (16.8 MB W^UK; 16.8 MB W^UV + 235 MB W^O) against the measured HBM rate."""
+    from mla_latent_kv_71_b300 import mla
+    dev = torch.device("cuda", local)
+    spec = workloads.WORKLOADS["mtp_b32_t2_l8192"]
+    B, T, H, d_h, d_c, d = spec["B"], spec["T"], spec["H"], spec["d_h"], spec["d_c"], spec["d"]
+    rows = B * T
+    bf = torch.bfloat16
+    w_uk, w_uv, w_o = workloads.projection_weights(H, d_h, d_c, d, seed=spec["seed"] + 4000, device=dev,
+                                                   dtype=bf)
+    qn = workloads.q_nope(B, T, H, d_h, seed=spec["seed"] + 3000, device=dev, dtype=bf).reshape(rows, H, d_h)
+    g = torch.Generator(device=dev).manual_seed(spec["seed"] + 5000)
+    o = torch.randn((rows, H, d_c), generator=g, device=dev).to(bf)
+    q_lat = torch.empty((rows, H, d_c), dtype=bf, device=dev)
+    v_tmp = torch.empty((rows, H * d_h), dtype=bf, device=dev)
+    out = torch.empty((rows, d), dtype=bf, device=dev)
+    ws = torch.zeros(max(1, mla.out_proj_workspace_size(rows, H, d_h, d, bf)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(s):
+            for _ in range(args.warmup):
+                fn()
+            times = []
+            for _ in range(args.steps):
+                flush.fill_(1)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(s)
+                fn()
+                b.record(s)
+                b.synchronize()
+                times.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(times)
+
+    pk, pk_kind = peaks()
+    res = {"metric": "MLA decode projections alone, weight GB/s vs measured HBM", "rows": rows, "H": H,
+           "d_h": d_h, "d_c": d_c, "d": d, "dtype": "bf16", "data": "synthetic",
+           "timing": f"median of {args.steps} single launches, L2 flushed before each",
+           "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
+    for name, fn, wbytes, other, flops in (
+            ("absorb_q", lambda: mla.absorb_q(qn, w_uk, q_lat, stream=s), w_uk.numel() * 2,
+             (qn.numel() + q_lat.numel()) * 2, 2 * rows * H * d_h * d_c),
+            ("out_proj", lambda: mla.out_proj(o, w_uv, w_o, v_tmp, out, ws, stream=s),
+             (w_uv.numel() + w_o.numel()) * 2, (o.numel() + 2 * v_tmp.numel() + out.numel()) * 2,
+             2 * rows * H * d_h * d_c + 2 * rows * d * H * d_h)):
+        us = timed(fn)
+        gbs = (wbytes + other) / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
+                     "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12}
+    code, detail = mla.get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail:#x}")
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,12 +530,18 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--projections", action="store_true",
+                    help="time mla_absorb_q and mla_out_proj alone (rows a1/a8)")
     ap.add_argument("--ref-step-s", type=float, default=5.0,
                     help="reference arm: CPU seconds per step (sample size)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     rank, world, local = dist_setup()
+    if args.projections:
+        if rank == 0:
+            print(json.dumps(run_projections(args, local)), flush=True)
+        return
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args, rank, world)), flush=True)
