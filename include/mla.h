@@ -131,9 +131,12 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
  * mla_decode_plan -- how mla_decode_attn (bf16) divides a batch over the GPU,
  * computed on the host from the same arithmetic the kernel uses.
  * The pages of all units u = (b*T + t)*ceil(H/128) + head_group are laid end
- * to end and cut into min(clusters, total pages) equal contiguous ranges, one
- * per 2-CTA cluster; a unit cut by a range boundary is computed in pieces
- * whose partial results are merged by log-sum-exp.
+ * to end on a line where each non-empty unit after the first is preceded by
+ * 3 virtual pages when the line holds at least 8 pages per cluster (starting
+ * a unit piece costs a cluster about that much), and the line is cut into
+ * min(clusters, total pages) equal contiguous ranges, one per 2-CTA cluster;
+ * a unit cut by a range boundary is computed in pieces whose partial results
+ * are merged by log-sum-exp.
  *   seq_lens_host [B] int32 (host), clusters: co-resident clusters (0 = the
  *   current device's value).
  *   out: up to `cap` rows of 7 int64: (cluster, unit, first page, end page

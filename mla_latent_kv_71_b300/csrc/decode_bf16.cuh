@@ -22,32 +22,37 @@
 // duplicated.
 //
 // The exchange (16 KB per tile each way) is slow next to the rest of a tile,
-// so it is pipelined: S and P are double-buffered in TMEM, and two groups of
-// four warps take alternate tiles.  Each group sends its partial S tile to
-// the peer (st.async from registers), receives the peer's, and runs the
-// softmax of its tile, so one tile's exchange overlaps the other's
-// exponentials.  The only serial hand-off between the groups is the running
-// maximum of each row (and, at the end of a unit, the row sums), passed
-// through shared memory.
+// so it is pipelined: two groups of four warps take alternate tiles, and a
+// group runs the front half of its next tile (own partial S out of TMEM and
+// off to the peer with st.async) before the back half of its current one
+// (the peer's partial in, online softmax, P into TMEM), so one tile's
+// exchange overlaps the other's exponentials.  The only serial hand-off
+// between the groups is the running maximum of each row (and, at the end of
+// a unit piece, the row sums), passed through shared memory.
 //
-// TMEM per CTA (512 columns allocated):
-//     [0,256)   O half, fp32          [256,320) S, 2 x 32 fp32 columns
-//     [320,352) P, 2 x 16 bf16 pairs  [352,496) Q half, bf16 pairs
-// Q and P are UMMA A operands read from TMEM; the page in shared memory is
-// the B operand of both products: K-major for S (features contiguous),
-// MN-major for O (the same bytes, read along the feature axis).
+// TMEM per CTA (all 512 columns):
+//     [0,256)   O half, fp32          [256,384) latent Q half, bf16 pairs
+//     [384,480) partial S, 3 x 32     [480,512) P, 2 x 16 bf16 pairs
+// Tile i's partial S sits in buffer i % 3 until the back half of the tile
+// has re-read it (so no tile's scores are carried in registers across the
+// front half of the next); its P goes to buffer i % 2.  The latent Q and P
+// are UMMA A operands read from TMEM; the RoPE part of Q (128 x 32) sits in
+// shared memory and feeds the two RoPE steps of S as an SS product.  The
+// page in shared memory is the B operand of both products: K-major for S
+// (features contiguous), MN-major for O (the same bytes, read along the
+// feature axis).
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warp 0      TMA producer: pages into a 4-stage ring (and zeroes the rows
 //               past the end of a partial last page),
 //   warp 1      TMEM owner; an elected lane issues each tile's S = Q.K^T as
-//               soon as its page has landed and its S buffer has been read,
+//               soon as its page has landed and its S buffer is free,
 //   warp 2      an elected lane issues each tile's O += P.C, in tile order,
 //               as soon as its P is in TMEM,
 //   warps 3..6  tiles 0, 2, 4, ...: partial S -> peer, peer's partial ->
 //               online softmax -> P into TMEM; lazy rescaling of O, the
-//               query of a unit that starts on their tile, the epilogue of
-//               a unit that ends on it,
+//               query of a unit piece that starts on their tile, the
+//               epilogue of one that ends on it,
 //   warps 7..10 the same for tiles 1, 3, 5, ...
 // The control warps wait with suspended (blocking) mbarrier waits, so they
 // take no issue slots from the tile groups that share their sub-partitions.
@@ -55,11 +60,12 @@
 // lane owns head row h of the tile.
 //
 // Work split: the pages of all (sequence, token, head-group) units are laid
-// end to end and cut into equal contiguous ranges, one per cluster, so long
-// and ragged sequences are spread over every SM.  A unit that straddles a
-// range boundary is finished by each cluster as a partial (normalised o and
-// its lse, fp32, in the workspace) and merged by a log-sum-exp combine
-// kernel launched after this one.
+// end to end, with a few virtual pages charged for each unit boundary, and
+// cut into equal contiguous ranges, one per cluster, so long and ragged
+// sequences are spread over every SM.  A unit that straddles a range
+// boundary is finished by each cluster as a partial (normalised o and its
+// lse, fp32, in the workspace) and merged by a log-sum-exp combine kernel
+// launched after this one.
 #pragma once
 
 #include <cstdint>
