@@ -217,11 +217,20 @@ def traffic_record(kernel_src_sha: str):
     return d.get("dram_bytes_per_launch"), d.get("source")
 
 
+def code_only(src: str) -> str:
+    """C++ source without comments and blank lines (the traffic record is
+    keyed by the code, so that editing a comment does not void it)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for name in ("decode_bf16.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "mla_latent_kv_71_b300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "mla_latent_kv_71_b300", "csrc", name)) as f:
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 
