@@ -184,11 +184,24 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                 if (*flag == 2) {  // last split of this tile: reduce in split order
                     __threadfence();
                     __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
-                    for (int n = 0; n < n_valid; ++n) {
-                        float acc = 0.f;
-                        for (int s = 0; s < p.splits; ++s)
-                            acc += __ldcg(p.ws_part + (((int64_t)s * Z + z) * p.N + n0 + n) * p.M + m);
-                        dst[(int64_t)(n0 + n) * p.ldo] = __float2bfloat16_rn(acc);
+                    // 8 columns at a time, each split's 8 loads issued together
+                    // (the sum still runs over the splits in order)
+                    for (int nb = 0; nb < n_valid; nb += 8) {
+                        float acc[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+#pragma unroll 4
+                        for (int s = 0; s < p.splits; ++s) {
+                            const float* src = p.ws_part + (((int64_t)s * Z + z) * p.N + n0 + nb) * p.M + m;
+                            float v[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) v[j] = nb + j < n_valid ? __ldcg(src + (int64_t)j * p.M) : 0.f;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) acc[j] += v[j];
+                        }
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (nb + j < n_valid) dst[(int64_t)(n0 + nb + j) * p.ldo] = __float2bfloat16_rn(acc[j]);
                     }
                     if (threadIdx.x == 0) p.ws_count[tile] = 0;
                 }
