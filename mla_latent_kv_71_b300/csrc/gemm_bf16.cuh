@@ -32,7 +32,7 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int STAGES = 4;  // pipeline depth (fewer when a CTA has fewer K chunks)
 constexpr int THREADS = 128;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB per stage
 
@@ -44,6 +44,7 @@ struct Params {
     int x_batched;        // X has a head coordinate (z); else z = 0 for X
     int splits;           // split-K factor (grid.z)
     int chunks_per_split; // K chunks (of BK) per split
+    int stages;           // pipeline stages in shared memory, 1..STAGES
     __nv_bfloat16* out;   // out[(n0+n) * ldo + z * out_z + m0 + m]
     int64_t ldo, out_z;
     float* ws_part;       // [splits][Z][N][M] fp32 partials (split-K only)
@@ -52,7 +53,10 @@ struct Params {
 
 __device__ __forceinline__ uint32_t x_bytes(int BN) { return (uint32_t)BN * BK * 2; }
 
-__global__ void __launch_bounds__(THREADS, 1)
+// At most 128 registers, so that up to four CTAs fit an SM when the
+// pipeline is short (a short K leaves each CTA little to load: more CTAs in
+// flight hide the TMA round trip).
+__global__ void __launch_bounds__(THREADS, 4)
 wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_x,
              const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -60,9 +64,10 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t xb = x_bytes(p.BN);
     const uint32_t stage_bytes = A_BYTES + xb;  // multiple of 1024 (BN % 8 == 0)
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * stage_bytes);
+    const int S = p.stages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
     // bars[0..S): full, bars[S..2S): empty, bars[2S]: accumulator ready
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
     int* flag = reinterpret_cast<int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -76,10 +81,10 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     uint32_t tmem_cols = 32;
     while (tmem_cols < (uint32_t)p.BN) tmem_cols <<= 1;
 
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + STAGES);
-    const uint32_t acc_bar = smem_u32(bars + 2 * STAGES);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+    const uint32_t acc_bar = smem_u32(bars + 2 * S);
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
@@ -101,8 +106,8 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         const uint64_t pol = l2_policy_evict_first();
         int it = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++it) {
-            const int s = it % STAGES;
-            if (!mbar_wait(empty0 + 8 * s, ((it / STAGES) & 1) ^ 1, 0x101)) { ok = false; break; }
+            const int s = it % S;
+            if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) { ok = false; break; }
             const uint32_t sa = smem_u32(smem + s * stage_bytes);
             const uint32_t sx = sa + A_BYTES;
             mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
@@ -115,16 +120,16 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
             tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? z : 0, n0, pol);
         }
         if (!ok) {  // let every issued copy land before the CTA can exit
-            for (int i = max(0, it - STAGES); i < it; ++i)
-                mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1, 0x102);
+            for (int i = max(0, it - S); i < it; ++i)
+                mbar_wait(full0 + 8 * (i % S), (i / S) & 1, 0x102);
         }
     } else if (!skip && warp == 1 && lane == 0) {
         // --------------------------------------------------------------- MMA
         const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
         int it = 0;
         for (int kc = kc0; kc < kc1; ++kc, ++it) {
-            const int s = it % STAGES;
-            if (!mbar_wait(full0 + 8 * s, (it / STAGES) & 1, 0x103)) { ok = false; break; }
+            const int s = it % S;
+            if (!mbar_wait(full0 + 8 * s, (it / S) & 1, 0x103)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sa = smem_u32(smem + s * stage_bytes);
             const uint32_t sx = sa + A_BYTES;

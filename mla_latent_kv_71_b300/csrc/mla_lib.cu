@@ -207,13 +207,13 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tx, int M, in
     p.x_batched = x_batched;
     p.splits = g.splits;
     p.chunks_per_split = g.chunks;
+    p.stages = g.chunks < mla::gemm::STAGES ? (g.chunks > 0 ? g.chunks : 1) : mla::gemm::STAGES;
     p.out = out;
     p.ldo = ldo;
     p.out_z = out_z;
     p.ws_part = ws_part;
     p.ws_count = ws_count;
-    const size_t smem = (size_t)mla::gemm::STAGES * (mla::gemm::A_BYTES + g.BN * mla::gemm::BK * 2) +
-                        256 + 1024;
+    const size_t smem = (size_t)p.stages * (mla::gemm::A_BYTES + g.BN * mla::gemm::BK * 2) + 256 + 1024;
     dim3 grid(M / mla::gemm::BM, Z * g.n_tiles, g.splits);
     mla::gemm::wgemm_kernel<<<grid, mla::gemm::THREADS, smem, st>>>(ta, tx, p);
     return launch_status();
