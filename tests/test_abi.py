@@ -61,3 +61,22 @@ def test_bad_sizes_are_rejected_on_the_host():
     assert lib.mla_combine_splits(fake, fake, 2, 1, 6, fake, fake, mla.MLA_BF16, None) == 1
     misaligned = ctypes.c_void_p((1 << 20) + 2)
     assert lib.mla_absorb_q(misaligned, fake, fake, 1, 1, 128, 512, mla.MLA_BF16, None) == 1
+
+
+def test_shapes_the_bf16_kernels_do_not_cover_are_refused_on_the_host():
+    # MLA_ERR_UNSUPPORTED (2), returned before any launch: widths or page size
+    # other than the kernel's, a pool beyond 32-bit row indices, and a plan
+    # whose 32-bit arithmetic would overflow (units x (pages per unit + 3)).
+    lib = mla.library()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def call(B=1, T=1, H=128, d_c=512, d_r=64, page=64, max_pages=1, num_pages=1):
+        return lib.mla_decode_attn(fake, fake, fake, fake, fake, None, B, T, H, d_c, d_r, page,
+                                   max_pages, num_pages, 0.07, 0, fake, fake, fake, 1 << 30,
+                                   mla.MLA_BF16, None)
+
+    assert call(d_c=256) == 2
+    assert call(d_r=32) == 2
+    assert call(page=32) == 2
+    assert call(num_pages=(1 << 31) // 64 + 1) == 2
+    assert call(B=1 << 19, max_pages=4096) == 2  # 2^19 units x 4099 > 2^31
