@@ -304,7 +304,7 @@ def test_full_size_end_to_end_sampled(name):
     # from the bf16 q_nope, decode from the GPU's bf16 q_lat, out_proj from the
     # GPU's o.  Then the fp64 chain from q_nope, compared on the final output
     # (q_lat and o are stored in bf16 between the stages, which moves lse by
-    # up to a few 1e-3 for short sequences; the chain is judged on out).
+    # up to a few 1e-3 for short sequences; the chain is checked on out).
     bs = [0, B - 1]
     sub = workloads.DecodeCase(q_lat[bs], case.q_pe[bs], case.pool, case.page_table[bs],
                                case.seq_lens[bs], case.scale, case.causal)

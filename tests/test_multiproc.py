@@ -4,7 +4,7 @@ The decode path has no exchange step, so more GPUs mean independent
 replicas: each rank times its own replica, rank 0 prints the one JSON line,
 and the step time is the maximum over ranks.  These tests run that host
 logic as two processes on the CPU -- the helpers directly, and the whole
-reference arm launched the way the N > 1 driver launches bench.py."""
+reference arm launched as a multi-GPU run launches bench.py (torch.distributed.run)."""
 
 import json
 import os
