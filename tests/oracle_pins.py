@@ -139,6 +139,33 @@ def pin_naive_equals_absorbed(lib):
     assert np.abs(out_n).max() > 1e-3  # not a vacuous zero
 
 
+
+def pin_naive_equals_absorbed_at_model_widths(lib):
+    """(a) again, at the DeepSeek-V2/V3 widths the GPU path runs (d_c = 512,
+    d_h = 128, d_r = 64, d = 7168), with two causal query tokens, bf16 inputs
+    and a paged, permuted cache on the absorbed side.
+
+    A subsample (2 sequences of 130 rows, 4 heads) keeps the naive route,
+    which expands K and V for every head, to a second of CPU.  Same passages
+    as the tiny-model check: reassociating the products changes no result.
+    """
+    B, T, H, d_h, d_c, d_r, d, L = 2, 2, 4, 128, 512, 64, 7168, 130
+    case = workloads.decode_case(B, T, H, d_c, d_r, [L] * B, seed=21, d_h=d_h)
+    w_uk, w_uv, w_o = workloads.projection_weights(H, d_h, d_c, d, seed=22)
+    q_nope = workloads.q_nope(B, T, H, d_h, seed=23)
+    cache = torch.cat([_gather_kv(case, b) for b in range(B)]).numpy()  # [B*L, d_c+d_r]
+    u_n, out_n = oracle.naive_decode(cache, q_nope, case.q_pe, w_uk, w_uv, w_o, L,
+                                     case.scale, causal=True, lib=lib)
+    q_lat = oracle.absorb_q(q_nope.reshape(B * T, H, d_h), w_uk, lib=lib)
+    o, lse = oracle.decode_attn(q_lat.reshape(B, T, H, d_c), case.q_pe, case.pool,
+                                case.page_table, case.seq_lens, case.scale, causal=True,
+                                lib=lib)
+    out_a, u_a = oracle.out_proj(o.reshape(B * T, H, d_c), w_uv, w_o, lib=lib)
+    assert _rel(u_a.reshape(u_n.shape), u_n) < 1e-12
+    assert _rel(out_a.reshape(out_n.shape), out_n) < 1e-12
+    assert np.abs(out_n).max() > 1e-2  # not a vacuous zero
+
+
 def pin_naive_vs_library_sdpa(lib):
     """The naive route's attention equals torch's fp64 SDPA on the expanded K, V.
 
@@ -274,6 +301,32 @@ def pin_softmax_rows_sum_to_one(lib):
                 assert abs(a.sum() - 1.0) < 1e-14 and (a >= 0).all()
 
 
+
+def pin_fp64_rounding_is_negligible(lib):
+    """The oracle's fp64 rounding is far below every tolerance it serves.
+
+    One 4096-row sequence with 1 % of its latent rows scaled by 8 (the
+    long-context workload's hot rows) is decoded by the oracle and, from the
+    definition (softmax of the scaled scores, latent-weighted sum, natural-log
+    lse), in numpy's extended precision (64-bit significand on x86): the two
+    agree to about 1e-14, eleven orders of magnitude inside the bf16 bars.
+    """
+    case = workloads.decode_case(1, 1, 2, 512, 64, [4096], seed=24, hot_frac=0.01)
+    o, lse = oracle.decode_attn(case.q_lat, case.q_pe, case.pool, case.page_table,
+                                case.seq_lens, case.scale, lib=lib)
+    ld = np.longdouble
+    rows = _gather_kv(case, 0).numpy().astype(ld)                           # [n, 576]
+    q = torch.cat([case.q_lat[0, 0], case.q_pe[0, 0]], -1).double().numpy().astype(ld)
+    s = (q @ rows.T) * ld(case.scale)                                       # [H, n]
+    m = s.max(axis=1, keepdims=True)
+    w = np.exp(s - m)
+    ref_o = (w @ rows[:, :512]) / w.sum(axis=1, keepdims=True)
+    ref_lse = m[:, 0] + np.log(w.sum(axis=1))
+    assert np.finfo(ld).nmant >= 63  # an extended type, not a second double
+    assert float(np.abs(o[0, 0] - ref_o).max() / np.abs(ref_o).max()) < 1e-13
+    assert float(np.abs(lse[0, 0] - ref_lse).max()) < 1e-12
+
+
 def pin_page_permutation_invariance(lib):
     """Where the pages sit in the pool does not change the result (exactly)."""
     case = _small_case(lens=(17, 100, 64), seed=14)
@@ -364,8 +417,8 @@ def pin_bf16_widening(lib):
 
 ALL_PINS = [
     pin_cache_accounting, pin_absorption_cost, pin_rope, pin_naive_equals_absorbed,
-    pin_naive_vs_library_sdpa, pin_project_vs_library, pin_position_shift_invariance,
+    pin_naive_equals_absorbed_at_model_widths, pin_naive_vs_library_sdpa, pin_project_vs_library, pin_position_shift_invariance,
     pin_decode_vs_library_sdpa, pin_decode_closed_forms, pin_softmax_rows_sum_to_one,
-    pin_page_permutation_invariance, pin_combine_split_identity, pin_empty_sequence,
+    pin_fp64_rounding_is_negligible, pin_page_permutation_invariance, pin_combine_split_identity, pin_empty_sequence,
     pin_out_proj_vs_library, pin_bf16_widening,
 ]
