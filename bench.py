@@ -470,12 +470,37 @@ def run_reference(args, rank, world):
     }
 
 
+def time_alone(fn, s, flush, steps: int, warmup: int) -> float:
+    """Median device time (us) of one call of fn on stream s, L2 flushed
+    before each: fn is captured once in a CUDA graph and the graph replayed,
+    so the host's submission work (argument checks, tensor maps) stays
+    outside the timed region, as in the decode step's timing."""
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            fn()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        fn()
+    times = []
+    with torch.cuda.stream(s):
+        for _ in range(steps):
+            flush.fill_(1)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            graph.replay()
+            b.record(s)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(times)
+
+
 def run_projections(args, local):
     """The query absorption (q_lat = W^UK^T q_nope) and the output projection
     (out = W^O concat_i W^UV_i o_i) at the two-token workload's sizes (64
-    query rows x 128 heads, d_h 128, d_c 512, d 7168), each timed alone: CUDA
-    events around single launches, L2 flushed (a 256 MB write) before each,
-    median over the timed launches.  Both are bound by their weight bytes
+    query rows x 128 heads, d_h 128, d_c 512, d 7168), each timed alone: one
+    call captured in a CUDA graph, CUDA events around each replay, L2 flushed
+    (a 256 MB write) before each, median over the timed replays.  Both are bound by their weight bytes
     (16.8 MB W^UK; 16.8 MB W^UV + 235 MB W^O) against the measured HBM rate."""
     from mla_latent_kv_71_b300 import mla
     dev = torch.device("cuda", local)
@@ -496,24 +521,12 @@ def run_projections(args, local):
     s = torch.cuda.Stream(device=dev)
 
     def timed(fn):
-        with torch.cuda.stream(s):
-            for _ in range(args.warmup):
-                fn()
-            times = []
-            for _ in range(args.steps):
-                flush.fill_(1)
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(s)
-                fn()
-                b.record(s)
-                b.synchronize()
-                times.append(a.elapsed_time(b) * 1e3)
-        return statistics.median(times)
+        return time_alone(fn, s, flush, args.steps, args.warmup)
 
     pk, pk_kind = peaks()
     res = {"metric": "MLA decode projections alone, weight GB/s vs measured HBM", "rows": rows, "H": H,
            "d_h": d_h, "d_c": d_c, "d": d, "dtype": "bf16", "data": "synthetic",
-           "timing": f"median of {args.steps} single launches, L2 flushed before each",
+           "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
            "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
     for name, fn, wbytes, other, flops in (
             ("absorb_q", lambda: mla.absorb_q(qn, w_uk, q_lat, stream=s), w_uk.numel() * 2,
@@ -531,6 +544,69 @@ def run_projections(args, local):
     return res
 
 
+def run_prologue(args, local):
+    """The steps before the decode, each timed alone like --projections: the
+    cache write of one new token per sequence of the headline batch (64
+    tokens at position 4096: c = W^DKV h and k^R = RoPE(W^KR h) from d = 7168
+    into the paged pool) and the query of those tokens (W^Q c^Q from the
+    1536-wide compressed query to 128 heads x [128 content ; 64 RoPE],
+    RoPE part rotated).  Both are bound by their weight bytes (8.3 MB and
+    75.5 MB) against the measured HBM rate."""
+    from mla_latent_kv_71_b300 import mla
+    dev = torch.device("cuda", local)
+    B, pos, d, d_c, d_r, H, d_h, d_q = 64, 4096, 7168, 512, 64, 128, 128, 1536
+    bf = torch.bfloat16
+    g = torch.Generator(device=dev).manual_seed(6000)
+    w_dkv = workloads.weight((d_c, d), d, g, dev, bf)
+    w_kr = workloads.weight((d_r, d), d, g, dev, bf)
+    w_q = workloads.weight((H * (d_h + d_r), d_q), d_q, g, dev, bf)
+    h = torch.randn((B, d), generator=g, device=dev).to(bf)
+    c_q = torch.randn((B, d_q), generator=g, device=dev).to(bf)
+    seq_ids = torch.arange(B, dtype=torch.int32, device=dev)
+    positions = torch.full((B,), pos, dtype=torch.int32, device=dev)
+    max_pages = pos // workloads.PAGE + 1
+    table = torch.full((B, max_pages), -1, dtype=torch.int32, device=dev)
+    table[:, pos // workloads.PAGE] = torch.arange(B, dtype=torch.int32, device=dev)
+    pool = torch.zeros((B, workloads.PAGE, d_c + d_r), dtype=bf, device=dev)
+    ws_kv = torch.zeros(max(1, mla.cache_append_workspace_size(B, d, d_c, bf)), dtype=torch.uint8,
+                        device=dev)
+    ws_q = torch.zeros(max(1, mla.project_q_workspace_size(B, H, d_h, d_r, d_q, bf)),
+                       dtype=torch.uint8, device=dev)
+    q_nope = torch.empty((B, H, d_h), dtype=bf, device=dev)
+    q_pe = torch.empty((B, H, d_r), dtype=bf, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        return time_alone(fn, s, flush, args.steps, args.warmup)
+
+    pk, pk_kind = peaks()
+    res = {"metric": "MLA decode prologue alone, GB/s vs measured HBM", "tokens": B, "position": pos,
+           "d": d, "d_c": d_c, "d_r": d_r, "H": H, "d_h": d_h, "d_q": d_q, "dtype": "bf16",
+           "data": "synthetic", "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
+           "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
+    for name, fn, wbytes, other, flops, launches in (
+            ("cache_append",
+             lambda: mla.cache_append(h, w_dkv, w_kr, seq_ids, positions, table, pool, workspace=ws_kv,
+                                      stream=s),
+             (w_dkv.numel() + w_kr.numel()) * 2, h.numel() * 2 + B * (d_c + d_r) * 2,
+             2 * B * (d_c + d_r) * d, 2),
+            ("project_q",
+             lambda: mla.project_q(c_q, w_q, positions, H, d_h, d_r, q_nope, q_pe, workspace=ws_q,
+                                   stream=s),
+             w_q.numel() * 2, c_q.numel() * 2 + (q_nope.numel() + q_pe.numel()) * 2,
+             2 * B * H * (d_h + d_r) * d_q, 2)):
+        us = timed(fn)
+        gbs = (wbytes + other) / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
+                     "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12,
+                     "launches_per_call": launches}
+    code, detail = mla.get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail:#x}")
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -541,6 +617,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--projections", action="store_true",
                     help="time mla_absorb_q and mla_out_proj alone (rows a1/a8)")
+    ap.add_argument("--prologue", action="store_true",
+                    help="time mla_cache_append and mla_project_q alone (the cache write before the path)")
     ap.add_argument("--ref-step-s", type=float, default=5.0,
                     help="reference arm: CPU seconds per step (sample size)")
     args = ap.parse_args()
@@ -550,6 +628,10 @@ def main():
     if args.projections:
         if rank == 0:
             print(json.dumps(run_projections(args, local)), flush=True)
+        return
+    if args.prologue:
+        if rank == 0:
+            print(json.dumps(run_prologue(args, local)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

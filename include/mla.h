@@ -5,6 +5,8 @@
  * The decode step of one attention layer, for query token t of sequence b and
  * head i, against the cached rows [c_j ; k^R_j] of positions j:
  *
+ *   c_j = W^DKV h_j, k^R_j = RoPE(W^KR h_j), into the pool     mla_cache_append
+ *   q^C_i, q^R_i = W^Q h (per head), q^R_i rotated             mla_project_q
  *   q_lat_i = W^UK_i^T q^C_i                                   mla_absorb_q
  *   s_ij    = (q_lat_i . c_j + q^R_i . k^R_j) * scale          mla_decode_attn
  *   o_i     = sum_j softmax_j(s_ij) c_j,  lse_i = ln sum_j e^{s_ij}
@@ -190,6 +192,88 @@ size_t mla_out_proj_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t 
 mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void* v_tmp,
                           void* out, int rows, int H, int d_h, int d_c, int d, void* workspace,
                           size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * Bytes of device workspace mla_cache_append needs (0 for MLA_FP32): the
+ * c rows of the N tokens, then the tensor-core GEMM's split-K scratch.  The
+ * workspace must be zero-filled before its first use; every call leaves its
+ * counters at zero again.
+ */
+size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype);
+
+/*
+ * mla_cache_append -- the cache write of N new tokens, the step that feeds
+ * the decode: for token n with hidden state h_n at position pos_n of
+ * sequence s_n,
+ *     c   = W^DKV h_n                      (d -> d_c, the joint latent)
+ *     k^R = RoPE(W^KR h_n, pos_n)          (d -> d_r, shared by all heads)
+ * and the row [c ; k^R] is stored at row pos_n % page_size of pool page
+ * page_table[s_n][pos_n / page_size].
+ * ([Mishra] "Step 1: a low-rank latent": only c is cached; "Step 4:
+ * decoupled RoPE": the positional key is a separate small projection of h,
+ * rotated, one vector for all heads; [llms] "Low-Rank Key-Value Joint
+ * Compression" and "The Positional Problem and Decoupled RoPE".)
+ * RoPE rotates pair (x_2k, x_2k+1) by the angle pos * rope_base^(-2k/d_r)
+ * (y_2k = x_2k cos - x_2k+1 sin, y_2k+1 = x_2k sin + x_2k+1 cos; the pages
+ * fix only that the angle depends on the position), computed in fp64.
+ *
+ *   h          [N, d]                   hidden states of the new tokens
+ *   w_dkv      [d_c, d]                 W^DKV
+ *   w_kr       [d_r, d]                 W^KR
+ *   seq_ids    [N] int32 (device)       sequence of each token, < B
+ *   positions  [N] int32 (device)       position of each token in its
+ *                                       sequence, < max_pages * page_size
+ *   page_table [B, max_pages] int32     as for mla_decode_attn; the entries
+ *                                       the tokens land in must be valid
+ *   kv_pool    [num_pages, page_size, d_c + d_r]   written in place (only
+ *                                       the N rows named by the tokens)
+ *   workspace  >= mla_cache_append_workspace_size(N, d, d_c, dtype) bytes
+ * Two tokens must not name the same pool row.  A token whose sequence,
+ * position or page id is out of range is not written and raises the device
+ * status (MLA_ERR_DEVICE_BOUNDS); as after any device error, which of the
+ * call's other rows were written is then unspecified (no row outside the
+ * tokens' rows is touched).
+ * d_c and d_r even; bf16: d_c % 128 == 0, d % 64 == 0, d_r % 8 == 0;
+ * fp32: d % 4 == 0.
+ */
+mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr,
+                              const int32_t* seq_ids, const int32_t* positions,
+                              const int32_t* page_table, void* kv_pool, int N, int d, int d_c,
+                              int d_r, int B, int page_size, int max_pages, int64_t num_pages,
+                              double rope_base, void* workspace, size_t workspace_bytes,
+                              mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * Bytes of device workspace mla_project_q needs (0 for MLA_FP32); same
+ * zero-fill rule as mla_cache_append_workspace_size.
+ */
+size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype);
+
+/*
+ * mla_project_q -- the query of N tokens, split per head and rotated:
+ *     q = W^Q h_n;  head i takes rows i*(d_h+d_r) .. (i+1)*(d_h+d_r)-1,
+ *     the first d_h as q^C_i (-> q_nope), the last d_r as q^R_i, which is
+ *     rotated at position pos_n (-> q_pe), with the RoPE of mla_cache_append
+ *     (in bf16 the sine and cosine of each angle, taken in fp64, are kept as
+ *     fp32 and the rotation is done in fp32).
+ * ([llms] "The Positional Problem and Decoupled RoPE": each head's query is
+ * the concatenation [q^C ; q^R] and only q^R is rotated; [Mishra] "Step 4:
+ * decoupled RoPE".)  h may be the model's hidden state (one W^Q) or the
+ * compressed query c^Q with W^Q = the stacked up-projections.
+ *
+ *   h         [N, d]                    input rows
+ *   w_q       [H * (d_h + d_r), d]      W^Q, per head [content ; RoPE] rows
+ *   positions [N] int32 (device)        position of each token
+ *   q_nope    [N, H, d_h]               output, the content query q^C
+ *   q_pe      [N, H, d_r]               output, the rotated RoPE query
+ *   workspace >= mla_project_q_workspace_size(N, H, d_h, d_r, d, dtype)
+ * d_h and d_r even; bf16: H*(d_h+d_r) % 128 == 0, d % 64 == 0,
+ * d_h % 8 == 0, d_r % 8 == 0; fp32: d % 4 == 0.
+ */
+mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
+                           void* q_pe, int N, int H, int d_h, int d_r, int d, double rope_base,
+                           void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                           mla_stream_t stream);
 
 /*
  * Synchronise `stream`, then read and clear the current device's status

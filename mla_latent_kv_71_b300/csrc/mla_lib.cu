@@ -15,6 +15,7 @@
 #include "decode_bf16.cuh"
 #include "gemm_bf16.cuh"
 #include "kernels_fp32.cuh"
+#include "prologue.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 
@@ -173,7 +174,10 @@ struct GemmPlan {
     size_t ws_part_bytes, ws_count_bytes;
 };
 
-GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, bool allow_split) {
+// max_splits > 0 caps the split-K factor: the last CTA of a tile adds the
+// splits' partials serially, so a GEMM with few output tiles (a small M)
+// would otherwise spend longer reducing than streaming its weight.
+GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, bool allow_split, int max_splits = 0) {
     GemmPlan g;
     g.BN = N >= 256 ? 256 : ((N + 15) / 16) * 16;
     g.n_tiles = (N + g.BN - 1) / g.BN;
@@ -185,6 +189,7 @@ GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, bool allow_split) {
         splits = (target + tiles / 2) / tiles;
         if (splits < 1) splits = 1;
         if (splits > chunks_total) splits = chunks_total;
+        if (max_splits > 0 && splits > max_splits) splits = max_splits;
     }
     g.chunks = (chunks_total + splits - 1) / splits;
     g.splits = (chunks_total + g.chunks - 1) / g.chunks;
@@ -219,13 +224,44 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tx, int M, in
     return launch_status();
 }
 
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Split-K cap of the prologue's GEMMs (W^DKV h has only d_c / 128 output
+// tiles per token block).
+constexpr int kPrologueMaxSplits = 8;
+
+// Scratch of one plain GEMM: split-K partials, then the arrival counters
+// (zero before the first use; every call leaves them at zero).
+size_t plain_gemm_ws_bytes(const GemmPlan& g) { return round256(g.ws_part_bytes) + g.ws_count_bytes; }
+
+// out[n * ldo + m] = sum_k W[m, k] X[n, k] in bf16: the weight W [M, K]
+// (K-major) on the UMMA M axis, the activation rows X [N, K] on N.
+mla_status_t plain_gemm(const void* W, const void* X, __nv_bfloat16* out, int64_t ldo, int M, int N,
+                        int K, const GemmPlan& g, void* ws, cudaStream_t st) {
+    CUtensorMap ta, tx;
+    cuuint64_t ad[3] = {(cuuint64_t)K, (cuuint64_t)M, 1};
+    cuuint64_t as[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * M * 2};
+    cuuint32_t ab[3] = {64, 128, 1};
+    cuuint64_t xd[3] = {(cuuint64_t)K, 1, (cuuint64_t)N};
+    cuuint64_t xs[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * 2};
+    cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g.BN};
+    if (!make_map(&ta, W, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tx, X, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLA_ERR_CUDA;
+    float* ws_part = g.splits > 1 ? static_cast<float*>(ws) : nullptr;
+    int* ws_count = g.splits > 1
+                        ? reinterpret_cast<int*>(static_cast<char*>(ws) + round256(g.ws_part_bytes))
+                        : nullptr;
+    return launch_gemm(ta, tx, M, N, K, 1, 0, 0, g, out, ldo, 0, ws_part, ws_count, st);
+}
+
 }  // namespace
 
 // =================================================================== C ABI
 
 extern "C" {
 
-int mla_version(void) { return 100; }
+int mla_version(void) { return 101; }
 
 uint64_t mla_launch_count(void) { return g_launches.load(); }
 
@@ -367,6 +403,140 @@ mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void
     int* ws_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + part_bytes);
     return launch_gemm(ta2, tx2, d, rows, K2, 1, 0, 0, g2, static_cast<__nv_bfloat16*>(out), d, 0,
                        g2.splits > 1 ? ws_part : nullptr, g2.splits > 1 ? ws_count : nullptr, st);
+}
+
+// ------------------------------------------- mla_cache_append / mla_project_q
+
+size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || N < 1 || d < 64 || d_c < 128) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    const GemmPlan g = gemm_plan(d_c, N, d, 1, di.sms, true, kPrologueMaxSplits);
+    return round256(sizeof(__nv_bfloat16) * (size_t)N * d_c) + plain_gemm_ws_bytes(g);
+}
+
+mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr,
+                              const int32_t* seq_ids, const int32_t* positions,
+                              const int32_t* page_table, void* kv_pool, int N, int d, int d_c,
+                              int d_r, int B, int page_size, int max_pages, int64_t num_pages,
+                              double rope_base, void* workspace, size_t workspace_bytes,
+                              mla_dtype_t dtype, mla_stream_t stream) {
+    if (!h || !w_dkv || !w_kr || !seq_ids || !positions || !page_table || !kv_pool)
+        return MLA_ERR_INVALID_ARG;
+    if (N < 1 || d < 1 || d_c < 2 || d_r < 2 || (d_c % 2) != 0 || (d_r % 2) != 0 || B < 1 ||
+        page_size < 1 || max_pages < 1 || num_pages < 1 || !(rope_base > 0.0))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(kv_pool))
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    mla::pro::KvParams p;
+    p.h = h;
+    p.w_dkv = w_dkv;
+    p.w_kr = w_kr;
+    p.c_tmp = nullptr;
+    p.seq_ids = seq_ids;
+    p.positions = positions;
+    p.page_table = page_table;
+    p.pool = kv_pool;
+    p.N = N;
+    p.d = d;
+    p.d_c = d_c;
+    p.d_r = d_r;
+    p.B = B;
+    p.page = page_size;
+    p.max_pages = max_pages;
+    p.num_pages = num_pages;
+    p.rope_base = rope_base;
+    const unsigned gx = (unsigned)((N + mla::pro::TOK - 1) / mla::pro::TOK);
+    if (dtype == MLA_FP32) {
+        if (d % 4 != 0) return MLA_ERR_UNSUPPORTED;
+        p.e_first = 0;
+        const dim3 grid(gx, (unsigned)((d_c + d_r + mla::pro::ROWS - 1) / mla::pro::ROWS));
+        mla::pro::kv_rows_kernel<float><<<grid, mla::pro::THREADS, 0, st>>>(p);
+        return launch_status();
+    }
+    if (d_c % 128 != 0 || d % 64 != 0 || d_r % 8 != 0) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const GemmPlan g = gemm_plan(d_c, N, d, 1, di.sms, true, kPrologueMaxSplits);
+    const size_t c_bytes = round256(sizeof(__nv_bfloat16) * (size_t)N * d_c);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < c_bytes + plain_gemm_ws_bytes(g))
+        return MLA_ERR_INVALID_ARG;
+    // c = W^DKV h on the tensor cores into the workspace, then W^KR h, the
+    // rotation and the scatter of whole rows into the pool
+    __nv_bfloat16* c_tmp = static_cast<__nv_bfloat16*>(workspace);
+    mla_status_t s = plain_gemm(w_dkv, h, c_tmp, d_c, d_c, N, d, g,
+                                static_cast<char*>(workspace) + c_bytes, st);
+    if (s != MLA_OK) return s;
+    p.c_tmp = c_tmp;
+    p.e_first = d_c;
+    const dim3 grid(gx, (unsigned)((d_r + mla::pro::ROWS - 1) / mla::pro::ROWS));
+    mla::pro::kv_rows_kernel<__nv_bfloat16><<<grid, mla::pro::THREADS, 0, st>>>(p);
+    return launch_status();
+}
+
+size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || N < 1 || H < 1 || d_h < 1 || d_r < 1 || d < 64) return 0;
+    const int64_t M = (int64_t)H * (d_h + d_r);
+    if (M % 128 != 0 || M > (1 << 30)) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, true, kPrologueMaxSplits);
+    return round256(sizeof(__nv_bfloat16) * (size_t)N * (size_t)M) + plain_gemm_ws_bytes(g);
+}
+
+mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
+                           void* q_pe, int N, int H, int d_h, int d_r, int d, double rope_base,
+                           void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                           mla_stream_t stream) {
+    if (!h || !w_q || !positions || !q_nope || !q_pe) return MLA_ERR_INVALID_ARG;
+    if (N < 1 || H < 1 || d_h < 2 || d_r < 2 || (d_h % 2) != 0 || (d_r % 2) != 0 || d < 1 ||
+        !(rope_base > 0.0))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(h) || !aligned16(w_q) || !aligned16(q_nope) || !aligned16(q_pe))
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    const int64_t M = (int64_t)H * (d_h + d_r);
+    if (M > (1 << 30)) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    mla::pro::QParams p;
+    p.h = h;
+    p.w_q = w_q;
+    p.q_tmp = nullptr;
+    p.positions = positions;
+    p.q_nope = q_nope;
+    p.q_pe = q_pe;
+    p.N = N;
+    p.d = d;
+    p.H = H;
+    p.d_h = d_h;
+    p.d_r = d_r;
+    p.rope_base = rope_base;
+    if (dtype == MLA_FP32) {
+        const int64_t gy = (M + mla::pro::ROWS - 1) / mla::pro::ROWS;
+        if (d % 4 != 0 || gy > 65535) return MLA_ERR_UNSUPPORTED;
+        const dim3 grid((unsigned)((N + mla::pro::TOK - 1) / mla::pro::TOK), (unsigned)gy);
+        mla::pro::q_rows_fp32_kernel<<<grid, mla::pro::THREADS, 0, st>>>(p);
+        return launch_status();
+    }
+    if (M % 128 != 0 || d % 64 != 0 || d_h % 8 != 0 || d_r % 8 != 0 || d_r > 8192)
+        return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, true, kPrologueMaxSplits);
+    const size_t q_bytes = round256(sizeof(__nv_bfloat16) * (size_t)N * (size_t)M);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < q_bytes + plain_gemm_ws_bytes(g))
+        return MLA_ERR_INVALID_ARG;
+    // q = W^Q h on the tensor cores into the workspace, then the split per
+    // head and the rotation of the RoPE part
+    __nv_bfloat16* q_tmp = static_cast<__nv_bfloat16*>(workspace);
+    mla_status_t s = plain_gemm(w_q, h, q_tmp, M, (int)M, N, d, g,
+                                static_cast<char*>(workspace) + q_bytes, st);
+    if (s != MLA_OK) return s;
+    p.q_tmp = q_tmp;
+    mla::pro::q_split_bf16_kernel<<<(unsigned)N, mla::pro::THREADS, sizeof(float) * (size_t)d_r, st>>>(p);
+    return launch_status();
 }
 
 // ---------------------------------------------------------- mla_combine

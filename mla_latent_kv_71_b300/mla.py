@@ -25,7 +25,9 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "M
 SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_combine_splits",
            "mla_out_proj_workspace_size", "mla_out_proj", "mla_get_device_status",
            "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count",
-           "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes"]
+           "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes",
+           "mla_cache_append_workspace_size", "mla_cache_append", "mla_project_q_workspace_size",
+           "mla_project_q"]
 
 
 class MLAError(RuntimeError):
@@ -77,6 +79,15 @@ def _lib():
         lib.mla_decode_attn_noalloc.restype = I
         lib.mla_decode_noalloc_max_bytes.argtypes = []
         lib.mla_decode_noalloc_max_bytes.restype = Z
+        D = ctypes.c_double
+        lib.mla_cache_append_workspace_size.argtypes = [I, I, I, I]
+        lib.mla_cache_append_workspace_size.restype = Z
+        lib.mla_cache_append.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, L, D, P, Z, I, P]
+        lib.mla_cache_append.restype = I
+        lib.mla_project_q_workspace_size.argtypes = [I, I, I, I, I, I]
+        lib.mla_project_q_workspace_size.restype = Z
+        lib.mla_project_q.argtypes = [P, P, P, P, P, I, I, I, I, I, D, P, Z, I, P]
+        lib.mla_project_q.restype = I
         _LIB = lib
     return _LIB
 
@@ -224,6 +235,62 @@ def out_proj(o, w_uv, w_o, v_tmp=None, out=None, workspace=None, stream=None):
         _ptr(o), _ptr(w_uv), _ptr(w_o), _ptr(v_tmp), _ptr(out), rows, H, d_h, d_c, d,
         _ptr(workspace), ws_bytes, _dt(o), _stream(stream)))
     return out
+
+
+def cache_append_workspace_size(N: int, d: int, d_c: int, dtype=torch.bfloat16) -> int:
+    return int(_lib().mla_cache_append_workspace_size(
+        N, d, d_c, MLA_BF16 if dtype == torch.bfloat16 else MLA_FP32))
+
+
+def cache_append(h, w_dkv, w_kr, seq_ids, positions, page_table, kv_pool,
+                 rope_base: float = 10000.0, workspace=None, stream=None):
+    """Write [W^DKV h_n ; RoPE(W^KR h_n, pos_n)] for each token n into its pool row.
+
+    h [N,d], w_dkv [d_c,d], w_kr [d_r,d], seq_ids / positions [N] int32,
+    page_table [B,max_pages] int32, kv_pool [num_pages,page,d_c+d_r]
+    (updated in place).  Returns kv_pool.
+    """
+    N, d = h.shape
+    d_c, d_r = w_dkv.shape[0], w_kr.shape[0]
+    B, max_pages = page_table.shape
+    num_pages, page, _ = kv_pool.shape
+    need = cache_append_workspace_size(N, d, d_c, h.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=h.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_cache_append", _lib().mla_cache_append(
+        _ptr(h), _ptr(w_dkv), _ptr(w_kr), _ptr(seq_ids), _ptr(positions), _ptr(page_table),
+        _ptr(kv_pool), N, d, d_c, d_r, B, page, max_pages, num_pages, float(rope_base),
+        _ptr(workspace), ws_bytes, _dt(h), _stream(stream)))
+    return kv_pool
+
+
+def project_q_workspace_size(N: int, H: int, d_h: int, d_r: int, d: int,
+                             dtype=torch.bfloat16) -> int:
+    return int(_lib().mla_project_q_workspace_size(
+        N, H, d_h, d_r, d, MLA_BF16 if dtype == torch.bfloat16 else MLA_FP32))
+
+
+def project_q(h, w_q, positions, H: int, d_h: int, d_r: int, q_nope=None, q_pe=None,
+              rope_base: float = 10000.0, workspace=None, stream=None):
+    """q = W^Q h per head [q^C ; q^R], q^R rotated at each token's position.
+
+    h [N,d], w_q [H*(d_h+d_r),d], positions [N] int32.  Returns
+    (q_nope [N,H,d_h], q_pe [N,H,d_r]).
+    """
+    N, d = h.shape
+    if q_nope is None:
+        q_nope = torch.empty((N, H, d_h), dtype=h.dtype, device=h.device)
+    if q_pe is None:
+        q_pe = torch.empty((N, H, d_r), dtype=h.dtype, device=h.device)
+    need = project_q_workspace_size(N, H, d_h, d_r, d, h.dtype)
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=h.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_project_q", _lib().mla_project_q(
+        _ptr(h), _ptr(w_q), _ptr(positions), _ptr(q_nope), _ptr(q_pe), N, H, d_h, d_r, d,
+        float(rope_base), _ptr(workspace), ws_bytes, _dt(h), _stream(stream)))
+    return q_nope, q_pe
 
 
 def get_device_status(stream=None) -> tuple[int, int]:

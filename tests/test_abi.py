@@ -80,3 +80,33 @@ def test_shapes_the_bf16_kernels_do_not_cover_are_refused_on_the_host():
     assert call(page=32) == 2
     assert call(num_pages=(1 << 31) // 64 + 1) == 2
     assert call(B=1 << 19, max_pages=4096) == 2  # 2^19 units x 4099 > 2^31
+
+
+def test_prologue_calls_reject_bad_arguments_on_the_host():
+    lib = mla.library()
+    fake = ctypes.c_void_p(1 << 20)
+
+    def append(d=7168, d_c=512, d_r=64, N=4, dtype=mla.MLA_BF16, h=fake, pool=fake):
+        return lib.mla_cache_append(h, fake, fake, fake, fake, fake, pool, N, d, d_c, d_r, 2, 64,
+                                    4, 8, 10000.0, fake, 1 << 30, dtype, None)
+
+    def project(d=1536, H=128, d_h=128, d_r=64, N=4, dtype=mla.MLA_BF16, q_pe=fake):
+        return lib.mla_project_q(fake, fake, fake, fake, q_pe, N, H, d_h, d_r, d, 10000.0, fake,
+                                 1 << 30, dtype, None)
+
+    for dtype in (mla.MLA_BF16, mla.MLA_FP32):
+        assert append(h=None, dtype=dtype) == 1
+        assert append(N=0, dtype=dtype) == 1
+        assert append(d_r=63, dtype=dtype) == 1              # RoPE needs pairs
+        assert append(pool=ctypes.c_void_p((1 << 20) + 4), dtype=dtype) == 1
+        assert project(q_pe=None, dtype=dtype) == 1
+        assert project(d_h=127, dtype=dtype) == 1
+    assert append(d_c=384 + 64) == 2                          # bf16: d_c % 128
+    assert append(d=7168 + 32) == 2                           # bf16: d % 64
+    assert append(d_r=36) == 2                                # bf16: d_r % 8
+    assert append(d=102, d_c=60, d_r=10, dtype=mla.MLA_FP32) == 2  # fp32: d % 4
+    assert project(H=3, d_h=6, d_r=4) == 2                    # bf16: H*(d_h+d_r) % 128
+    assert project(d=1536 + 32) == 2                          # bf16: d % 64
+    assert project(d=102, dtype=mla.MLA_FP32) == 2            # fp32: d % 4
+    assert lib.mla_cache_append_workspace_size(4, 7168, 512, mla.MLA_FP32) == 0
+    assert lib.mla_project_q_workspace_size(4, 128, 128, 64, 1536, mla.MLA_FP32) == 0
