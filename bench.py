@@ -607,6 +607,52 @@ def run_prologue(args, local):
     return res
 
 
+def run_merged(args, local):
+    """The output projection two ways at the two-token workload's sizes (64
+    rows, 128 heads, d_h 128, d_c 512, d 7168), each timed like
+    --projections: W^UV and W^O kept apart (mla_out_proj, 252 MB of
+    weights) and merged ahead of time (mla_out_proj_merged, one 7168 x 65536
+    matrix, 940 MB) -- the trade the pages weigh."""
+    from mla_latent_kv_71_b300 import mla
+    dev = torch.device("cuda", local)
+    spec = workloads.WORKLOADS["mtp_b32_t2_l8192"]
+    B, T, H, d_h, d_c, d = spec["B"], spec["T"], spec["H"], spec["d_h"], spec["d_c"], spec["d"]
+    rows = B * T
+    bf = torch.bfloat16
+    _, w_uv, w_o = workloads.projection_weights(H, d_h, d_c, d, seed=spec["seed"] + 4000, device=dev,
+                                                dtype=bf)
+    g = torch.Generator(device=dev).manual_seed(spec["seed"] + 5000)
+    o = torch.randn((rows, H, d_c), generator=g, device=dev).to(bf)
+    w_merged = mla.fold_out_weights(w_uv, w_o)
+    v_tmp = torch.empty((rows, H * d_h), dtype=bf, device=dev)
+    out = torch.empty((rows, d), dtype=bf, device=dev)
+    ws = torch.zeros(max(1, mla.out_proj_workspace_size(rows, H, d_h, d, bf)), dtype=torch.uint8, device=dev)
+    ws_m = torch.zeros(max(1, int(mla.library().mla_out_proj_merged_workspace_size(rows, H, d_c, d, 0))),
+                       dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    pk, pk_kind = peaks()
+    res = {"metric": "MLA output projection, weights kept apart vs merged, GB/s vs measured HBM",
+           "rows": rows, "H": H, "d_h": d_h, "d_c": d_c, "d": d, "dtype": "bf16", "data": "synthetic",
+           "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
+           "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
+    for name, fn, wbytes, other, flops in (
+            ("out_proj", lambda: mla.out_proj(o, w_uv, w_o, v_tmp, out, ws, stream=s),
+             (w_uv.numel() + w_o.numel()) * 2, (o.numel() + 2 * v_tmp.numel() + out.numel()) * 2,
+             2 * rows * H * d_h * d_c + 2 * rows * d * H * d_h),
+            ("out_proj_merged", lambda: mla.out_proj_merged(o, w_merged, out, ws_m, stream=s),
+             w_merged.numel() * 2, (o.numel() + out.numel()) * 2, 2 * rows * d * H * d_c)):
+        us = time_alone(fn, s, flush, args.steps, args.warmup)
+        gbs = (wbytes + other) / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
+                     "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12}
+    res["merged_over_apart_time"] = res["out_proj_merged"]["us"] / res["out_proj"]["us"]
+    code, detail = mla.get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail:#x}")
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -619,6 +665,8 @@ def main():
                     help="time mla_absorb_q and mla_out_proj alone (rows a1/a8)")
     ap.add_argument("--prologue", action="store_true",
                     help="time mla_cache_append and mla_project_q alone (the cache write before the path)")
+    ap.add_argument("--merged", action="store_true",
+                    help="time mla_out_proj against mla_out_proj_merged (W^O W^UV merged ahead of time)")
     ap.add_argument("--ref-step-s", type=float, default=5.0,
                     help="reference arm: CPU seconds per step (sample size)")
     args = ap.parse_args()
@@ -632,6 +680,10 @@ def main():
     if args.prologue:
         if rank == 0:
             print(json.dumps(run_prologue(args, local)), flush=True)
+        return
+    if args.merged:
+        if rank == 0:
+            print(json.dumps(run_merged(args, local)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

@@ -12,6 +12,8 @@
  *   o_i     = sum_j softmax_j(s_ij) c_j,  lse_i = ln sum_j e^{s_ij}
  *   (pieces of one softmax merged by log-sum-exp)              mla_combine_splits
  *   out     = W^O concat_i (W^UV_i o_i)                        mla_out_proj
+ *           (or with W^O W^UV merged ahead of time: mla_fold_out_weights,
+ *            mla_out_proj_merged)
  *
  * Sources (web pages on MLA):
  *   [Mishra] "Multi-head Latent Attention", Neel Mishra: sections "Step 2:
@@ -192,6 +194,46 @@ size_t mla_out_proj_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t 
 mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void* v_tmp,
                           void* out, int rows, int H, int d_h, int d_c, int d, void* workspace,
                           size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * mla_fold_out_weights -- the output side's weights merged ahead of time:
+ *     W_merged[n, i*d_c : (i+1)*d_c] = W^UV_i^T W^O[n, i*d_h : (i+1)*d_h]
+ * so that out = W_merged concat_i o_i = W^O concat_i (W^UV_i o_i).
+ * ([Zhang] "Value absorption: weight and sum first, project after": W^UV
+ * leaves the weighted sum, and W^O W^UV may be merged ahead of time, at
+ * nearly four times the weight bytes for DeepSeek-V3; [Mishra] "Step 2:
+ * absorb the up-projections".)  Done once, offline; the result serves
+ * mla_out_proj_merged.
+ *
+ *   w_uv     [H, d_h, d_c]     W^UV
+ *   w_o      [d, H*d_h]        W^O
+ *   w_merged [d, H*d_c]        output (dtype)
+ * Same kernels and limits as mla_absorb_q with rows = d (bf16: d_c % 128
+ * == 0, d_h % 64 == 0).
+ */
+mla_status_t mla_fold_out_weights(const void* w_uv, const void* w_o, void* w_merged, int H, int d_h,
+                                  int d_c, int d, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * Bytes of device workspace mla_out_proj_merged needs (0 for MLA_FP32);
+ * zero-filled before its first use, as for mla_out_proj.
+ */
+size_t mla_out_proj_merged_workspace_size(int rows, int H, int d_c, int d, mla_dtype_t dtype);
+
+/*
+ * mla_out_proj_merged -- the output projection with the merged weight:
+ *     out[r, :] = W_merged o[r, :, :] (all heads' latents, H*d_c long)
+ * The same result as mla_out_proj up to rounding, streaming d*H*d_c weights
+ * instead of H*d_h*(d_c + d): the trade the pages weigh.
+ *
+ *   o        [rows, H, d_c]    latent outputs of mla_decode_attn
+ *   w_merged [d, H*d_c]        from mla_fold_out_weights
+ *   out      [rows, d]         output (dtype)
+ * bf16: d % 128 == 0, d_c % 64 == 0.
+ */
+mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out, int rows, int H,
+                                 int d_c, int d, void* workspace, size_t workspace_bytes,
+                                 mla_dtype_t dtype, mla_stream_t stream);
 
 /*
  * Bytes of device workspace mla_cache_append needs (0 for MLA_FP32): the

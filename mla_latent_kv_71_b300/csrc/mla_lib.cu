@@ -306,6 +306,7 @@ mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int
     if (!aligned16(q_nope) || !aligned16(w_uk) || !aligned16(q_lat)) return MLA_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dtype == MLA_FP32) {
+        if ((int64_t)rows * H > 0x7FFFFFFF) return MLA_ERR_UNSUPPORTED;
         dim3 grid((unsigned)rows * H, (d_c + 127) / 128);
         mla::absorb_q_fp32_kernel<<<grid, 128, 0, st>>>(
             static_cast<const float*>(q_nope), static_cast<const float*>(w_uk),
@@ -317,6 +318,7 @@ mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
     const GemmPlan g = gemm_plan(d_c, rows, d_h, H, di.sms, false);
+    if ((int64_t)H * g.n_tiles > 65535) return MLA_ERR_UNSUPPORTED;  // grid.y
     // A = W^UK_i^T, stored along d_c: MN-major tiles [64 d_h rows x 64 d_c]
     CUtensorMap ta, tx;
     cuuint64_t ad[3] = {(cuuint64_t)d_c, (cuuint64_t)d_h, (cuuint64_t)H};
@@ -403,6 +405,56 @@ mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void
     int* ws_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + part_bytes);
     return launch_gemm(ta2, tx2, d, rows, K2, 1, 0, 0, g2, static_cast<__nv_bfloat16*>(out), d, 0,
                        g2.splits > 1 ? ws_part : nullptr, g2.splits > 1 ? ws_count : nullptr, st);
+}
+
+// ------------------------------------------------- merged output weight
+
+mla_status_t mla_fold_out_weights(const void* w_uv, const void* w_o, void* w_merged, int H, int d_h,
+                                  int d_c, int d, mla_dtype_t dtype, mla_stream_t stream) {
+    if (!w_uv || !w_o || !w_merged || H < 1 || d_h < 1 || d_c < 1 || d < 1)
+        return MLA_ERR_INVALID_ARG;
+    // W_merged[n, i, :] = W^UV_i^T W^O[n, i, :] is the query absorption's
+    // product with row n of W^O, head slice i, in the place of q^C.
+    return mla_absorb_q(w_o, w_uv, w_merged, d, H, d_h, d_c, dtype, stream);
+}
+
+size_t mla_out_proj_merged_workspace_size(int rows, int H, int d_c, int d, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || rows < 1 || H < 1 || d_c < 1 || d < 128) return 0;
+    const int64_t K = (int64_t)H * d_c;
+    if (K > (1 << 30)) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, true));
+}
+
+mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out, int rows, int H,
+                                 int d_c, int d, void* workspace, size_t workspace_bytes,
+                                 mla_dtype_t dtype, mla_stream_t stream) {
+    if (!o || !w_merged || !out || rows < 1 || H < 1 || d_c < 1 || d < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(o) || !aligned16(w_merged) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    const int64_t K = (int64_t)H * d_c;
+    if (K > (1 << 30)) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == MLA_FP32) {
+        const int64_t warps = (int64_t)rows * d;
+        mla::out_proj_o_fp32_kernel<<<(unsigned)((warps + 3) / 4), 128, 0, st>>>(
+            static_cast<const float*>(o), static_cast<const float*>(w_merged), static_cast<float*>(out),
+            rows, (int)K, d);
+        return launch_status();
+    }
+    if (dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (d % 128 != 0 || d_c % 64 != 0) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, true);
+    if (g.splits > 1 &&
+        (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g)))
+        return MLA_ERR_INVALID_ARG;
+    // out = W_merged o on the tensor cores: the merged weight on the UMMA M
+    // axis, the rows of o (all heads' latents, H * d_c long) on N
+    return plain_gemm(w_merged, o, static_cast<__nv_bfloat16*>(out), d, d, rows, (int)K, g, workspace,
+                      st);
 }
 
 // ------------------------------------------- mla_cache_append / mla_project_q

@@ -27,7 +27,8 @@ SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_
            "mla_status_string", "mla_version", "mla_set_decode_events", "mla_launch_count",
            "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes",
            "mla_cache_append_workspace_size", "mla_cache_append", "mla_project_q_workspace_size",
-           "mla_project_q"]
+           "mla_project_q", "mla_fold_out_weights", "mla_out_proj_merged_workspace_size",
+           "mla_out_proj_merged"]
 
 
 class MLAError(RuntimeError):
@@ -88,6 +89,12 @@ def _lib():
         lib.mla_project_q_workspace_size.restype = Z
         lib.mla_project_q.argtypes = [P, P, P, P, P, I, I, I, I, I, D, P, Z, I, P]
         lib.mla_project_q.restype = I
+        lib.mla_fold_out_weights.argtypes = [P, P, P, I, I, I, I, I, P]
+        lib.mla_fold_out_weights.restype = I
+        lib.mla_out_proj_merged_workspace_size.argtypes = [I, I, I, I, I]
+        lib.mla_out_proj_merged_workspace_size.restype = Z
+        lib.mla_out_proj_merged.argtypes = [P, P, P, I, I, I, I, P, Z, I, P]
+        lib.mla_out_proj_merged.restype = I
         _LIB = lib
     return _LIB
 
@@ -234,6 +241,33 @@ def out_proj(o, w_uv, w_o, v_tmp=None, out=None, workspace=None, stream=None):
     _check("mla_out_proj", _lib().mla_out_proj(
         _ptr(o), _ptr(w_uv), _ptr(w_o), _ptr(v_tmp), _ptr(out), rows, H, d_h, d_c, d,
         _ptr(workspace), ws_bytes, _dt(o), _stream(stream)))
+    return out
+
+
+def fold_out_weights(w_uv, w_o, w_merged=None, stream=None):
+    """W_merged [d, H*d_c] with row n, head slice i = W^UV_i^T W^O[n, i*d_h:(i+1)*d_h]."""
+    H, d_h, d_c = w_uv.shape
+    d = w_o.shape[0]
+    if w_merged is None:
+        w_merged = torch.empty((d, H * d_c), dtype=w_uv.dtype, device=w_uv.device)
+    _check("mla_fold_out_weights", _lib().mla_fold_out_weights(
+        _ptr(w_uv), _ptr(w_o), _ptr(w_merged), H, d_h, d_c, d, _dt(w_uv), _stream(stream)))
+    return w_merged
+
+
+def out_proj_merged(o, w_merged, out=None, workspace=None, stream=None):
+    """out = W_merged concat_i o_i; o [rows,H,d_c], w_merged [d,H*d_c]."""
+    rows, H, d_c = o.shape
+    d = w_merged.shape[0]
+    if out is None:
+        out = torch.empty((rows, d), dtype=o.dtype, device=o.device)
+    need = int(_lib().mla_out_proj_merged_workspace_size(rows, H, d_c, d, _dt(o)))
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=o.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_out_proj_merged", _lib().mla_out_proj_merged(
+        _ptr(o), _ptr(w_merged), _ptr(out), rows, H, d_c, d, _ptr(workspace), ws_bytes, _dt(o),
+        _stream(stream)))
     return out
 
 

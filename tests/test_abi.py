@@ -110,3 +110,15 @@ def test_prologue_calls_reject_bad_arguments_on_the_host():
     assert project(d=102, dtype=mla.MLA_FP32) == 2            # fp32: d % 4
     assert lib.mla_cache_append_workspace_size(4, 7168, 512, mla.MLA_FP32) == 0
     assert lib.mla_project_q_workspace_size(4, 128, 128, 64, 1536, mla.MLA_FP32) == 0
+
+
+def test_merged_output_calls_reject_bad_arguments_on_the_host():
+    lib = mla.library()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.mla_fold_out_weights(None, fake, fake, 128, 128, 512, 7168, mla.MLA_BF16, None) == 1
+    assert lib.mla_fold_out_weights(fake, fake, fake, 128, 128, 500, 7168, mla.MLA_BF16, None) == 2
+    assert lib.mla_out_proj_merged(fake, None, fake, 64, 128, 512, 7168, fake, 1 << 30,
+                                   mla.MLA_BF16, None) == 1
+    assert lib.mla_out_proj_merged(fake, fake, fake, 64, 128, 512, 7100, fake, 1 << 30,
+                                   mla.MLA_BF16, None) == 2   # bf16: d % 128
+    assert lib.mla_out_proj_merged_workspace_size(64, 128, 512, 7168, mla.MLA_FP32) == 0

@@ -1,0 +1,77 @@
+"""The output projection with W^O W^UV merged ahead of time
+(mla_fold_out_weights, mla_out_proj_merged) against the fp64 oracle's
+unmerged out_proj (needs a B300).
+
+Merging is an exact reassociation ([Zhang] "Value absorption: weight and
+sum first, project after"), so the merged path must meet the same bars as
+the unmerged one: fp32 max abs 1e-4; bf16 |out - out*| <= 2e-2 + 2^-8 |out*|
+and relative Frobenius <= 5e-3.  (The merged weight is itself rounded to
+bf16 once, which adds about one bf16 rounding to the relative error.)
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_latent_kv_71_b300 import mla, workloads
+
+pytestmark = pytest.mark.gpu
+
+FP32_MAX, O_MAX, O_FRO, REL = 1e-4, 2e-2, 5e-3, 2.0 ** -8
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    mla.library()
+    yield
+
+
+@pytest.fixture(autouse=True)
+def _device_status():
+    mla.get_device_status()
+    yield
+    code, detail = mla.get_device_status()
+    assert code == 0, f"device status {code}: site {detail & 0xFFF:#x}"
+
+
+def test_fp32_merged_out_proj_tiny_widths():
+    rows, H, d_h, d_c, d = 5, 8, 32, 64, 256
+    w_uv_, w_o_ = workloads.projection_weights(H, d_h, d_c, d, seed=70, dtype=torch.float32)[1:]
+    o = torch.randn((rows, H, d_c), generator=torch.Generator().manual_seed(71))
+    w_merged = mla.fold_out_weights(w_uv_.cuda(), w_o_.cuda())
+    out = mla.out_proj_merged(o.cuda(), w_merged)
+    torch.cuda.synchronize()
+    ref, _ = oracle.out_proj(o, w_uv_, w_o_)
+    assert np.abs(out.cpu().double().numpy() - ref).max() <= FP32_MAX
+
+
+def test_bf16_merged_out_proj_model_widths():
+    """64 rows, 16 heads of d_h 128 / d_c 512, d = 7168: the merged weight is
+    7168 x 8192 (3.7x the bytes of W^UV and W^O kept apart)."""
+    rows, H, d_h, d_c, d = 64, 16, 128, 512, 7168
+    _, w_uv_, w_o_ = workloads.projection_weights(H, d_h, d_c, d, seed=72)
+    o = torch.randn((rows, H, d_c), generator=torch.Generator().manual_seed(73)).to(torch.bfloat16)
+    w_merged = mla.fold_out_weights(w_uv_.cuda(), w_o_.cuda())
+    out = mla.out_proj_merged(o.cuda(), w_merged)
+    torch.cuda.synchronize()
+    ref, _ = oracle.out_proj(o, w_uv_, w_o_)
+    got = out.float().cpu().double().numpy()
+    excess = (np.abs(got - ref) - (O_MAX + REL * np.abs(ref))).max()
+    fro = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert excess <= 0, f"max |out - out*| = {np.abs(got - ref).max():.3e}"
+    assert fro <= O_FRO, f"rel Frobenius = {fro:.3e}"
+    # the fold itself, on sampled entries, against the fp64 product of the
+    # bf16 weights
+    g = torch.Generator().manual_seed(74)
+    n = torch.randint(0, d, (64,), generator=g).tolist()
+    i = torch.randint(0, H, (64,), generator=g).tolist()
+    c = torch.randint(0, d_c, (64,), generator=g).tolist()
+    wm = w_merged.cpu().double()
+    for nk, ik, ck in zip(n, i, c):
+        exact = float((w_o_[nk, ik * d_h:(ik + 1) * d_h].double() * w_uv_[ik, :, ck].double()).sum())
+        assert abs(float(wm[nk, ik * d_c + ck]) - exact) <= REL * abs(exact) + 1e-6
