@@ -275,8 +275,8 @@ size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype)
  * status (MLA_ERR_DEVICE_BOUNDS); as after any device error, which of the
  * call's other rows were written is then unspecified (no row outside the
  * tokens' rows is touched).
- * d_c and d_r even; bf16: d_c % 128 == 0, d % 64 == 0, d_r % 8 == 0;
- * fp32: d % 4 == 0.
+ * d_r even (MLA_ERR_INVALID_ARG otherwise); d_c even; bf16: d_c % 128 == 0,
+ * d % 64 == 0, d_r % 8 == 0; fp32: d % 4 == 0.
  */
 mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr,
                               const int32_t* seq_ids, const int32_t* positions,
@@ -309,8 +309,9 @@ size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_d
  *   q_nope    [N, H, d_h]               output, the content query q^C
  *   q_pe      [N, H, d_r]               output, the rotated RoPE query
  *   workspace >= mla_project_q_workspace_size(N, H, d_h, d_r, d, dtype)
- * d_h and d_r even; bf16: H*(d_h+d_r) % 128 == 0, d % 64 == 0,
- * d_h % 8 == 0, d_r % 8 == 0; fp32: d % 4 == 0.
+ * d_r even (MLA_ERR_INVALID_ARG otherwise); d_h even; bf16:
+ * H*(d_h+d_r) % 128 == 0, d % 64 == 0, d_h % 8 == 0, d_r % 8 == 0;
+ * fp32: d % 4 == 0.
  */
 mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
                            void* q_pe, int N, int H, int d_h, int d_r, int d, double rope_base,

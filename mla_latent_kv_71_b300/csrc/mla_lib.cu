@@ -475,12 +475,14 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
                               mla_dtype_t dtype, mla_stream_t stream) {
     if (!h || !w_dkv || !w_kr || !seq_ids || !positions || !page_table || !kv_pool)
         return MLA_ERR_INVALID_ARG;
-    if (N < 1 || d < 1 || d_c < 2 || d_r < 2 || (d_c % 2) != 0 || (d_r % 2) != 0 || B < 1 ||
-        page_size < 1 || max_pages < 1 || num_pages < 1 || !(rope_base > 0.0))
+    // RoPE rotates pairs: an odd d_r has no meaning
+    if (N < 1 || d < 1 || d_c < 1 || d_r < 2 || (d_r % 2) != 0 || B < 1 || page_size < 1 ||
+        max_pages < 1 || num_pages < 1 || !(rope_base > 0.0))
         return MLA_ERR_INVALID_ARG;
     if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(kv_pool))
         return MLA_ERR_INVALID_ARG;
     if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (d_c % 2 != 0) return MLA_ERR_UNSUPPORTED;  // the kernels' row tiles keep RoPE pairs whole
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     mla::pro::KvParams p;
     p.h = h;
@@ -543,12 +545,13 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
                            void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
                            mla_stream_t stream) {
     if (!h || !w_q || !positions || !q_nope || !q_pe) return MLA_ERR_INVALID_ARG;
-    if (N < 1 || H < 1 || d_h < 2 || d_r < 2 || (d_h % 2) != 0 || (d_r % 2) != 0 || d < 1 ||
-        !(rope_base > 0.0))
+    // RoPE rotates pairs: an odd d_r has no meaning
+    if (N < 1 || H < 1 || d_h < 1 || d_r < 2 || (d_r % 2) != 0 || d < 1 || !(rope_base > 0.0))
         return MLA_ERR_INVALID_ARG;
     if (!aligned16(h) || !aligned16(w_q) || !aligned16(q_nope) || !aligned16(q_pe))
         return MLA_ERR_INVALID_ARG;
     if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (d_h % 2 != 0) return MLA_ERR_UNSUPPORTED;  // the kernels' row tiles keep RoPE pairs whole
     const int64_t M = (int64_t)H * (d_h + d_r);
     if (M > (1 << 30)) return MLA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -100,7 +100,9 @@ def test_prologue_calls_reject_bad_arguments_on_the_host():
         assert append(d_r=63, dtype=dtype) == 1              # RoPE needs pairs
         assert append(pool=ctypes.c_void_p((1 << 20) + 4), dtype=dtype) == 1
         assert project(q_pe=None, dtype=dtype) == 1
-        assert project(d_h=127, dtype=dtype) == 1
+        assert project(d_r=63, dtype=dtype) == 1
+        assert project(d_h=127, dtype=dtype) == 2           # RoPE pairs must not straddle tiles
+        assert append(d_c=511, dtype=dtype) == 2
     assert append(d_c=384 + 64) == 2                          # bf16: d_c % 128
     assert append(d=7168 + 32) == 2                           # bf16: d % 64
     assert append(d_r=36) == 2                                # bf16: d_r % 8
