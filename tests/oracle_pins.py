@@ -104,6 +104,16 @@ def pin_rope(lib):
     d1 = oracle.rope(q, 50, lib=lib) @ oracle.rope(k, 20, lib=lib)
     d2 = oracle.rope(q, 1050, lib=lib) @ oracle.rope(k, 1020, lib=lib)
     assert abs(d1 - d2) < 1e-9 * max(1.0, abs(d1))
+    # at the long-context positions the cache write uses (up to 131071):
+    # rotations compose, R(a) R(b) = R(a + b), and the relative score holds
+    x64 = rng.standard_normal(64)
+    a, b = 100000, 31071
+    assert np.abs(oracle.rope(oracle.rope(x64, a, lib=lib), b, lib=lib)
+                  - oracle.rope(x64, a + b, lib=lib)).max() < 1e-9
+    q, k = rng.standard_normal(64), rng.standard_normal(64)
+    d1 = oracle.rope(q, 7, lib=lib) @ oracle.rope(k, 3, lib=lib)
+    d2 = oracle.rope(q, 131071, lib=lib) @ oracle.rope(k, 131067, lib=lib)
+    assert abs(d1 - d2) < 1e-8 * max(1.0, abs(d1))
 
 
 # ------------------------------------------------------------ tiny fp32 model
