@@ -44,6 +44,13 @@ MUTANTS = {
     "query_rope_at_zero": ("d_r, (double)qpos, rope_base);", "d_r, 0.0, rope_base);"),
     "softmax_denominator": ("double a = exp(s[j] - m) / l;\n        if (a_out)",
                             "double a = exp(s[j] - m) / (l + 1.0);\n        if (a_out)"),
+    "cache_rope_at_zero": ("orc_rope(row + d_c, d_r, (double)j, rope_base);",
+                           "orc_rope(row + d_c, d_r, 0.0, rope_base);"),
+    "query_head_rows_pe_first": (
+        "if (e < d_h) q_nope[((int64_t)b * H + i) * d_h + e] = acc;\n"
+        "                else q_pe[((int64_t)b * H + i) * d_r + (e - d_h)] = acc;",
+        "if (e >= d_r) q_nope[((int64_t)b * H + i) * d_h + (e - d_r)] = acc;\n"
+        "                else q_pe[((int64_t)b * H + i) * d_r + e] = acc;"),
     "project_kr_uses_w_dkv": ("acc += rd(w_kr, dw2, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);",
                               "acc += rd(w_dkv, dw1, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);"),
 }
