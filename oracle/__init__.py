@@ -17,6 +17,10 @@ Parity status of each function (what pins it is listed in the tests):
   decode_attn ................. pinned by a library routine (SDPA), closed
                                 forms, invariants and the naive route
   combine ..................... pinned by the split identity
+  weight_spread ............... (test infrastructure: the sensitivity of o
+                                to rounding the weights, used by the parity
+                                bar) pinned by closed forms and by perturbing
+                                the weights
   project, naive_decode ....... pinned by a library routine (SDPA) and the
                                 identity against the absorbed route
 """
@@ -78,6 +82,8 @@ def _declare(lib):
     lib.orc_absorb_q.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P]
     lib.orc_decode_attn.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                     _I, _I, _D, _I, _P, _L, _P, _P]
+    lib.orc_weight_spread.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                      _I, _I, _D, _I, _P, _L, _P]
     lib.orc_attention_weights.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I,
                                           _I, _I, _D, _I, _I, _I, _I, _P]
     lib.orc_attention_weights.restype = _L
@@ -203,6 +209,33 @@ def decode_attn(q_lat, q_pe, pool, page_table, seq_lens, scale, causal=False, se
     if sel is None:
         return o.reshape(B, T, H, d_c), lse.reshape(B, T, H)
     return o, lse
+
+
+def weight_spread(q_lat, q_pe, pool, page_table, seq_lens, scale, causal=False, sel=None,
+                  lib=None):
+    """D[.., c] = sum_j a_j |c_j[c] - o[c]| for every (b, t, i), or for the
+    flattened indices in sel: how far o can move when the weights a_j are
+    perturbed by relative errors of at most u (by u / (1 - u) * D).  Not a
+    step of the method: the parity bar uses it to bound what rounding the
+    softmax weights to bf16 can do.  Shapes as decode_attn's o."""
+    lib = lib or load()
+    ql, dql = _arr(q_lat)
+    qp, dqp = _arr(q_pe)
+    pl, dp = _arr(pool)
+    pt = _i32(page_table)
+    sl = _i32(seq_lens)
+    B, T, H, d_c = ql.shape
+    d_r = qp.shape[3]
+    if sel is None:
+        n, sel_arr = B * T * H, None
+    else:
+        sel_arr = np.ascontiguousarray(sel, dtype=np.int64)
+        n = sel_arr.shape[0]
+    D = np.empty((n, d_c), dtype=np.float64)
+    lib.orc_weight_spread(_ptr(ql), dql, _ptr(qp), dqp, _ptr(pl), dp, _ptr(pt), _ptr(sl), B, T, H,
+                          d_c, d_r, pl.shape[1], pt.shape[1], float(scale), int(bool(causal)),
+                          _ptr(sel_arr) if sel_arr is not None else None, n, _ptr(D))
+    return D.reshape(B, T, H, d_c) if sel is None else D
 
 
 def attention_weights(q_lat, q_pe, pool, page_table, seq_lens, scale, b, t, i,

@@ -221,6 +221,58 @@ void orc_decode_attn(const void* q_lat, int dql, const void* q_pe, int dqp,
 }
 
 /*
+ * Sensitivity of o to rounding the attention weights (test infrastructure,
+ * not a step of the method).  For every listed (b, t, i) and latent column c
+ *     D[c] = sum_j a_j |c_j[c] - o[c]|
+ * with a_j and o of decode_one.  If every weight is perturbed to
+ * a_j (1 + e_j) and the weights renormalised, o moves by
+ *     sum_j a_j (e_j - ebar) c_j / (1 + ebar) = sum_j a_j e_j (c_j - o) / (1 + ebar)
+ * (ebar = sum_j a_j e_j), so |e_j| <= u moves o[c] by at most
+ * u / (1 - u) * D[c].  Rounding the weights to bf16 has u = 2^-8.
+ * sel as in orc_decode_attn (NULL: every row); D [rows, d_c].
+ */
+void orc_weight_spread(const void* q_lat, int dql, const void* q_pe, int dqp,
+                       const void* pool, int dp, const int32_t* page_table,
+                       const int32_t* seq_lens, int B, int T, int H, int d_c,
+                       int d_r, int page, int max_pages, double scale, int causal,
+                       const int64_t* sel, int64_t n_sel, double* D) {
+    int64_t total = sel ? n_sel : (int64_t)B * T * H;
+    int64_t max_len = 0;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] > max_len) max_len = seq_lens[b];
+    int64_t width = (int64_t)d_c + d_r;
+    #pragma omp parallel
+    {
+        size_t cap = (size_t)(max_len > 0 ? max_len : 1);
+        double* s = (double*)malloc(sizeof(double) * cap);
+        double* a = (double*)malloc(sizeof(double) * cap);
+        double* o = (double*)malloc(sizeof(double) * (size_t)d_c);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t k = 0; k < total; ++k) {
+            int64_t f = sel ? sel[k] : k;
+            int i = (int)(f % H);
+            int t = (int)((f / H) % T);
+            int b = (int)(f / ((int64_t)H * T));
+            int64_t n = visible_len(seq_lens[b], T, t, causal);
+            double lse;
+            decode_one(q_lat, dql, q_pe, dqp, pool, dp, page_table, n, b, t, i,
+                       T, H, d_c, d_r, page, max_pages, scale, s, o, &lse, a);
+            double* dst = D + k * d_c;
+            for (int c = 0; c < d_c; ++c) dst[c] = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t pg = page_table[(int64_t)b * max_pages + j / page];
+                int64_t row = (pg * page + j % page) * width;
+                for (int c = 0; c < d_c; ++c)
+                    dst[c] += a[j] * fabs(rd(pool, dp, row + c) - o[c]);
+            }
+        }
+        free(s);
+        free(a);
+        free(o);
+    }
+}
+
+/*
  * Attention weights a_j of one (b, t, i): the softmax row the decode uses.
  * [Zhang] "Value absorption": softmax over the scaled scores gives A(i, j).
  * a_out receives the n visible weights; returns n.

@@ -425,10 +425,53 @@ def pin_bf16_widening(lib):
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
 
 
+def pin_weight_spread(lib):
+    """The rounding sensitivity D = sum_j a_j |c_j - o| (test infrastructure):
+    0 for one cached row and for equal rows; for q = 0 (uniform weights) the
+    mean absolute deviation about the mean (numpy); and the largest change of
+    o under weight errors of at most u, found by perturbing the weights
+    directly, is u D to first order (reached by e_j = u sign(c_j - o))."""
+    case = _small_case(lens=(1, 50, 64), seed=31)
+    d_c = case.q_lat.shape[3]
+    args = (case.q_lat, case.q_pe, case.pool, case.page_table, case.seq_lens, case.scale)
+    D = oracle.weight_spread(*args, lib=lib)
+    o, _ = oracle.decode_attn(*args, lib=lib)
+    assert np.abs(D[0]).max() < 1e-14  # a single row: o = c_0
+    u = 2.0 ** -8
+    g = np.random.default_rng(3)
+    for b, i in [(1, 0), (2, 3)]:
+        rows = _gather_kv(case, b)[:, :d_c].numpy()
+        a = oracle.attention_weights(*args[:5], case.scale, b, 0, i, lib=lib)
+        for _ in range(3):  # random errors stay within u / (1 - u) D
+            e = g.uniform(-u, u, a.shape)
+            w = a * (1 + e)
+            o2 = (w / w.sum()) @ rows
+            assert (np.abs(o2 - o[b, 0, i]) <= u / (1 - u) * D[b, 0, i] + 1e-12).all()
+        for c in (0, d_c // 2, d_c - 1):  # the worst sign pattern reaches u D / (1 + ebar)
+            e = u * np.sign(rows[:, c] - o[b, 0, i, c])
+            w = a * (1 + e)
+            moved = abs(((w / w.sum()) @ rows[:, c]) - o[b, 0, i, c])
+            assert abs(moved * (1 + (a * e).sum()) - u * D[b, 0, i, c]) <= 1e-12 * (1 + D[b, 0, i, c])
+    zero = _small_case(lens=(1, 50, 64), seed=31)
+    zero.q_lat.zero_()
+    zero.q_pe.zero_()
+    Dz = oracle.weight_spread(zero.q_lat, zero.q_pe, zero.pool, zero.page_table, zero.seq_lens,
+                              zero.scale, lib=lib)
+    for b in (1, 2):
+        rows = _gather_kv(zero, b)[:, :d_c].numpy()
+        mad = np.abs(rows - rows.mean(0)).mean(0)
+        assert np.abs(Dz[b, 0] - mad).max() < 1e-13
+    same = _small_case(lens=(5, 40, 64), seed=32)
+    same.pool[:] = same.pool[0, 0]
+    Ds = oracle.weight_spread(same.q_lat, same.q_pe, same.pool, same.page_table, same.seq_lens,
+                              same.scale, lib=lib)
+    assert np.abs(Ds).max() < 1e-13
+
+
 ALL_PINS = [
     pin_cache_accounting, pin_absorption_cost, pin_rope, pin_naive_equals_absorbed,
     pin_naive_equals_absorbed_at_model_widths, pin_naive_vs_library_sdpa, pin_project_vs_library, pin_position_shift_invariance,
     pin_decode_vs_library_sdpa, pin_decode_closed_forms, pin_softmax_rows_sum_to_one,
     pin_fp64_rounding_is_negligible, pin_page_permutation_invariance, pin_combine_split_identity, pin_empty_sequence,
-    pin_out_proj_vs_library, pin_bf16_widening,
+    pin_out_proj_vs_library, pin_bf16_widening, pin_weight_spread,
 ]

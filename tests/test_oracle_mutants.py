@@ -51,6 +51,10 @@ MUTANTS = {
         "                else q_pe[((int64_t)b * H + i) * d_r + (e - d_h)] = acc;",
         "if (e >= d_r) q_nope[((int64_t)b * H + i) * d_h + (e - d_r)] = acc;\n"
         "                else q_pe[((int64_t)b * H + i) * d_r + e] = acc;"),
+    "spread_without_abs": ("dst[c] += a[j] * fabs(rd(pool, dp, row + c) - o[c]);",
+                           "dst[c] += a[j] * (rd(pool, dp, row + c) - o[c]);"),
+    "spread_about_zero": ("dst[c] += a[j] * fabs(rd(pool, dp, row + c) - o[c]);",
+                          "dst[c] += a[j] * fabs(rd(pool, dp, row + c));"),
     "project_kr_uses_w_dkv": ("acc += rd(w_kr, dw2, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);",
                               "acc += rd(w_dkv, dw1, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);"),
 }
