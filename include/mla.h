@@ -132,6 +132,34 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
                              size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream);
 
 /*
+ * mla_decode_attn_partial -- mla_decode_attn with o written in fp32 whatever
+ * the input type (dtype MLA_BF16 reads bf16 q_lat, q_pe and kv_pool; fp32
+ * mode is mla_decode_attn itself), for attention over one part of a
+ * sequence's cache whose result is merged with the other parts' later.
+ * o is then that part's normalised result and lse its log-sum-exp; the
+ * parts of one softmax merge exactly by
+ *     lse = ln sum_s e^{lse_s},   o = sum_s e^{lse_s - lse} o_s
+ * (mla_combine_splits), since the softmax over all positions weights each
+ * part's normalised result by that part's share of the total.  This is the
+ * exchange of one long sequence sharded by token range over several GPUs
+ * ([llms] "Hardware Trade-offs and Tensor Parallelism": the latent must be
+ * split or communicated across GPUs): each GPU runs this call on the pages
+ * it holds, the (o, lse) pairs are all-gathered, and mla_combine_splits
+ * merges them.  A part a query sees nothing of gives o = 0, lse = -inf,
+ * which the merge weighs by 0.
+ *
+ *   o    [B, T, H, d_c] fp32 output; other arguments as mla_decode_attn
+ *   workspace >= mla_decode_workspace_size(B, T, H, d_c, dtype) bytes
+ */
+mla_status_t mla_decode_attn_partial(const void* q_lat, const void* q_pe, const void* kv_pool,
+                                     const int32_t* page_table, const int32_t* seq_lens,
+                                     const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                                     int d_r, int page_size, int max_pages, int64_t num_pages,
+                                     float scale, int causal, float* o, float* lse,
+                                     void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                                     mla_stream_t stream);
+
+/*
  * mla_decode_plan -- how mla_decode_attn (bf16) divides a batch over the GPU,
  * computed on the host from the same arithmetic the kernel uses.
  * The pages of all units u = (b*T + t)*ceil(H/128) + head_group are laid end
@@ -327,6 +355,19 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
 mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail);
 
 /*
+ * Set how long a kernel of this library waits for a pipeline step (a page
+ * copy, a tensor-core product, a peer CTA) before it gives up, raises
+ * MLA_ERR_TIMEOUT in the device status word and winds down: `ns`
+ * nanoseconds on the current device, or the default of 2 s when ns == 0.
+ * The waits a CTA makes at teardown for copies and products it issued
+ * itself keep their own limit, so a short limit never leaves work in
+ * flight.  A very short limit makes calls fail with MLA_ERR_TIMEOUT; it is
+ * meant for testing the failure path.  Synchronous; returns MLA_ERR_CUDA if
+ * the write fails.  Not thread-safe against calls in flight.
+ */
+mla_status_t mla_set_wait_limit(uint64_t ns);
+
+/*
  * Timing hook: while set (both non-NULL), every bf16 mla_decode_attn call
  * records `start` on its stream just before its attention kernel and `end`
  * just after it, so that a caller can time that kernel apart from the
@@ -351,8 +392,16 @@ void mla_set_decode_events(void* start, void* end);
  * until the process exits.  (The web pages on MLA have no counterpart to
  * this call; it is an interface convenience.)
  *
- * The first call on a device looks up that array's device address (once
- * per device, with the device current); make that first call before any
+ * The array is 64 MiB.  The scratch needs (G + U) * 256 KiB plus a little,
+ * for U = B * T * ceil(H / 128) work units and G co-resident clusters (74
+ * on a 148-SM B300), so up to about 181 units fit on a B300: every decode
+ * batch of one token and 128 heads up to B = 181 (the 64-, 128- and
+ * 4-sequence batches, the 32 x 2-token batch and the 64 x 16-head batch all
+ * fit); 4 sequences of 64 query tokens do not.
+ *
+ * The first call on a device (and the first call after that device's CUDA
+ * context has been replaced, as by cudaDeviceReset) looks up that array's
+ * device address with the device current; make that first call before any
  * stream capture.  Every call shares the one array and overwrites what the
  * last call left there, so calls whose kernels overlap on the GPU (on
  * different streams, or from different host threads) race: serialise them.

@@ -96,7 +96,7 @@ constexpr uint32_t XT_BYTES = HEADS * TILE * 4;                   // one partial
 constexpr uint32_t OFF_STAGE = 0;
 constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [group][slot]
 constexpr uint32_t OFF_PUB = OFF_X + 4 * XT_BYTES;  // per-row state handed between the groups
-constexpr uint32_t PUB_BYTES = 2 * 3 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part][128]
+constexpr uint32_t PUB_BYTES = 2 * 4 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part, lr_part][128]
 // This CTA's 32 RoPE columns of the query (128 rows x 64 B, the layout a
 // 64-byte-swizzled TMA box would have): the A operand of the RoPE part of S.
 constexpr uint32_t OFF_QPE = OFF_PUB + PUB_BYTES;      // 1 KB aligned
@@ -131,7 +131,8 @@ struct Params {
     const __nv_bfloat16* q_pe;   // [B, T, H, 64]
     const int32_t* page_table;   // [B, max_pages]
     const int32_t* seq_lens;     // [B]
-    __nv_bfloat16* o;            // [B, T, H, 512]
+    __nv_bfloat16* o;            // [B, T, H, 512] bf16 output, or
+    float* o32;                  // [B, T, H, 512] fp32 output (exactly one is set)
     float* lse;                  // [B, T, H]
     float* ws_o;                 // [slots, 128, 512] normalised partial outputs
     float* ws_lse;               // [slots, 128]
@@ -426,7 +427,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     const uint32_t Q_FULL = BAR(30);                    // query of a unit in TMEM + smem (4 warps)
     const uint32_t O_FREE = BAR(31);                    // epilogue read O (4 warps)
     const uint32_t TAIL = BAR(32);                      // partial last page landed (TMA)
-    auto DRAIN = [&](int k) { return BAR(33 + k); };    // abort: MMAs of warp 1 + k finished
+    auto DRAIN = [&](int k) { return BAR(33 + k); };    // teardown: MMAs of warp 1 + k finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + OFF_MISC + 8);
 
@@ -621,11 +622,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 if (valid < PAGE) {
                     // Rows past the end may hold anything (even NaN); zero
                     // them so that P = 0 there cannot meet a NaN in P . C.
-                    ok = mbar_wait(TAIL, tail_phase, 0x202);
+                    // (The copy was issued here, so it is waited for even
+                    // when another CTA has raised the status word.)
+                    ok = mbar_wait_teardown(TAIL, tail_phase, MLA_WAIT_LIMIT_NS);
                     ok = __all_sync(0xffffffffu, ok);
                     tail_phase ^= 1u;
                     if (!ok) {
-                        ++it;  // the loads have landed; nothing is in flight
+                        raise_device_status(MLA_DEV_TIMEOUT, 0x202u | ((blockIdx.x & 0xFFFu) << 12));
+                        ++it;
                         break;
                     }
                     uint8_t* tile = smem + OFF_STAGE + s * STAGE_BYTES;
@@ -647,15 +651,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 }
             }
         }
-        if (!ok) {  // let every issued copy land before the CTA can exit
-            for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
-                mbar_wait(FULL((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), 0x203);
-        } else {
-            // Producer tail: the tensor core's last releases of the ring
-            // (tcgen05.commit arrivals) land before shared memory goes away.
-            for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
-                mbar_wait(EMPTY((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), 0x204);
-        }
+        // Every copy this warp issued lands before the CTA can exit, on the
+        // normal path (where these phases have completed long ago) and after
+        // an abort alike.  A partial page's FULL phase is this warp's own
+        // arrive, made above once its copy had landed.  (The tensor core's
+        // releases of the ring are waited for by the MMA warps themselves.)
+        for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
+            mbar_wait_teardown(FULL((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), MLA_WAIT_LIMIT_NS);
     } else if (warp == 1) {
         // ========================================================= MMA: S
         // The score products S = Q.K^T, tile by tile, each as soon as its
@@ -696,7 +698,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             issued = true;
             qk.advance(pv);
         }
-        if (!ok && issued) {  // wait for the tensor core before TMEM goes away
+        if (issued) {  // every product (and its commits) done before TMEM goes away
             if (elect_one_sync()) tc_commit(DRAIN(0));
             __syncwarp();
             mbar_wait_teardown(DRAIN(0), 0, MLA_WAIT_LIMIT_NS);
@@ -736,7 +738,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             issued = true;
             it.advance(pv);
         }
-        if (!ok && issued) {  // wait for the tensor core before TMEM goes away
+        if (issued) {  // every product (and its commits) done before TMEM goes away
             if (elect_one_sync()) tc_commit(DRAIN(1));
             __syncwarp();
             mbar_wait_teardown(DRAIN(1), 0, MLA_WAIT_LIMIT_NS);
@@ -757,14 +759,18 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         const uint32_t trow = tmem + ((uint32_t)(q4 * 32) << 16);
         const uint32_t peer_x0 = map_to_rank(smem_u32(smem + OFF_X + 2 * grp * XT_BYTES), peer);
         const uint32_t peer_xfull0 = map_to_rank(XFULL(2 * grp), peer);
-        float* pub = reinterpret_cast<float*>(smem + OFF_PUB);  // [2][3][HEADS]
+        float* pub = reinterpret_cast<float*>(smem + OFF_PUB);  // [2][4][HEADS]
         const bool leader = warp == WG_WARP0 + 4 * grp && lane == 0;
         const int my_g = (int)g_id;
         auto xslot = [](int i) { return (i >> 1) & 1; };
         auto xpar = [](int i) { return (uint32_t)((i >> 2) & 1); };
         auto s_par = [](int i) { return (uint32_t)((i / NS) & 1); };  // tile i's phase of its S buffer
         bool ok = !skip;
-        float m_ref = -INFINITY, l_part = 0.f;  // this group's row sum, relative to m_ref
+        // this group's row sums, relative to m_ref: of the exact exponentials
+        // (for lse) and of their bf16 roundings, the weights P . C applies
+        // (for o = P.C / lr: a weighted mean whose weights sum to exactly 1,
+        // so the rounding of a row that dominates the softmax cancels)
+        float m_ref = -INFINITY, l_part = 0.f, lr_part = 0.f;
         int64_t my_seg = -1;
         int64_t armed = misc[7 + grp], consumed = 0;
 
@@ -849,6 +855,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 my_seg = c.seg;
                 m_ref = -INFINITY;
                 l_part = 0.f;
+                lr_part = 0.f;
             }
             const int x = 2 * grp + xslot(i);
             if (!__all_sync(0xffffffffu, mbar_wait(XFULL(x), xpar(i), 0x504))) return false;
@@ -889,16 +896,17 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             if (i >= 1) {
                 if (!__all_sync(0xffffffffu, mbar_wait(M_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x505)))
                     return false;
-                m_prev = pub[(b ^ 1) * 3 * HEADS + h];
+                m_prev = pub[(b ^ 1) * 4 * HEADS + h];
             }
-            float m_oth = -INFINITY, l_oth = 0.f;  // the other group's sums (unit's last tile only)
+            float m_oth = -INFINITY, l_oth = 0.f, lr_oth = 0.f;  // the other group's sums (unit's last tile only)
             if (c.last && !c.first) {
                 // before this tile's maximum is published, so that the other
                 // group cannot publish its next tile's sums over these
                 if (!__all_sync(0xffffffffu, mbar_wait(L_PUB(b ^ 1), (uint32_t)(((i - 1) >> 1) & 1), 0x506)))
                     return false;
-                m_oth = pub[((b ^ 1) * 3 + 1) * HEADS + h];
-                l_oth = pub[((b ^ 1) * 3 + 2) * HEADS + h];
+                m_oth = pub[((b ^ 1) * 4 + 1) * HEADS + h];
+                l_oth = pub[((b ^ 1) * 4 + 2) * HEADS + h];
+                lr_oth = pub[((b ^ 1) * 4 + 3) * HEADS + h];
             }
             float m_used;
             bool need = false;
@@ -933,11 +941,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 tmem_st_wait();
                 tc_fence_before();
             }
-            pub[b * 3 * HEADS + h] = m_used;
+            pub[b * 4 * HEADS + h] = m_used;
             __syncwarp();
             if (lane == 0) mbar_arrive(M_PUB(b));
             if (m_ref != m_used) {  // this group's earlier sums, to the new reference
-                l_part = m_ref == -INFINITY ? 0.f : l_part * ex2(m_ref - m_used);
+                const float f = m_ref == -INFINITY ? 0.f : ex2(m_ref - m_used);
+                l_part *= f;
+                lr_part *= f;
                 m_ref = m_used;
             }
             // ---- P[b] is free once the tile two back has been multiplied
@@ -950,23 +960,25 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 uint32_t pk[TILE / 2];
                 const uint64_t nm2 = f2_pack(-m_used, -m_used);
                 const uint64_t c2 = f2_pack(p.scale_log2, p.scale_log2);
-                uint64_t sum2[2] = {0ull, 0ull};
+                uint64_t sum2 = 0ull, sumr2 = 0ull;
 #pragma unroll
                 for (int j = 0; j < TILE / 2; ++j) {
                     const uint64_t e = f2_fma(s2[j], c2, nm2);  // s * scale * log2(e) - m
                     const float p0 = ex2(f2_lo(e));
                     const float p1 = ex2(f2_hi(e));
-                    sum2[j & 1] = f2_add(sum2[j & 1], f2_pack(p0, p1));
                     pk[j] = pack_bf16x2(p0, p1);
+                    sum2 = f2_add(sum2, f2_pack(p0, p1));
+                    sumr2 = f2_add(sumr2, bf16x2_to_f2(pk[j]));
                 }
-                const uint64_t st = f2_add(sum2[0], sum2[1]);
-                l_part += f2_lo(st) + f2_hi(st);
+                l_part += f2_lo(sum2) + f2_hi(sum2);
+                lr_part += f2_lo(sumr2) + f2_hi(sumr2);
                 tmem_st16(trow + TM_P + 16 * b, pk);
             }
             tmem_st_wait();
             tc_fence_before();
-            pub[(b * 3 + 1) * HEADS + h] = m_ref;
-            pub[(b * 3 + 2) * HEADS + h] = l_part;
+            pub[(b * 4 + 1) * HEADS + h] = m_ref;
+            pub[(b * 4 + 2) * HEADS + h] = l_part;
+            pub[(b * 4 + 3) * HEADS + h] = lr_part;
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(P_FULL(b));
@@ -978,11 +990,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 // tile order).
                 if (!__all_sync(0xffffffffu, mbar_wait(PV_DONE(b), (uint32_t)((i >> 1) & 1), 0x509))) return false;
                 tc_fence_after();
-                const float l = l_part + (c.first ? 0.f : l_oth * ex2(m_oth - m_used));
+                const float f_oth = c.first ? 0.f : ex2(m_oth - m_used);
+                const float l = l_part + l_oth * f_oth;     // for lse
+                const float lr = lr_part + lr_oth * f_oth;  // for o
                 const int bt = c.u / p.HG;  // unit u = (b * T + t) * HG + hg
                 const int head0 = (c.u - bt * p.HG) * HEADS + q4 * 32;  // head of this warp's row 0
                 const int64_t qrow0 = (int64_t)bt * p.H + head0;
-                const float inv_l = 1.f / l;
+                const float inv_l = 1.f / lr;
                 // Rows go out through this tile's X buffer (the 4 KB this warp
                 // read): each thread puts its row's 16-byte chunks in, then the
                 // warp stores whole 64- or 128-byte row pieces per instruction
@@ -992,7 +1006,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 auto stg = [&](int r, int j) -> uint4* {
                     return reinterpret_cast<uint4*>(xbuf + j * (HEADS * 16) + q4 * 512 + 16 * ((r & 24) | ((r + j) & 7)));
                 };
-                if (c.slot < 0) {
+                if (c.slot < 0 && p.o32 == nullptr) {
                     __nv_bfloat16* dst = p.o + qrow0 * DC + rank * HALF_C + 8 * (lane & 3);
 #pragma unroll 1
                     for (int cc = 0; cc < HALF_C; cc += 32) {
@@ -1016,7 +1030,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                     }
                     if (head0 + lane < p.H && rank == 0) p.lse[qrow0 + lane] = (m_used + __log2f(l)) * LN2;
                 } else {
-                    float* dst = p.ws_o + (int64_t)(c.slot * HEADS + q4 * 32) * DC + rank * HALF_C + 4 * (lane & 7);
+                    // fp32 rows: the unit's partial result in its workspace
+                    // slot, or (fp32 output) the unit's own rows of o
+                    const bool direct = c.slot < 0;
+                    float* dst = (direct ? p.o32 + qrow0 * DC : p.ws_o + (int64_t)(c.slot * HEADS + q4 * 32) * DC) +
+                                 rank * HALF_C + 4 * (lane & 7);
+                    const int live_rows = direct ? min(32, p.H - head0) : 32;
 #pragma unroll 1
                     for (int cc = 0; cc < HALF_C; cc += 32) {
                         uint32_t r[32];
@@ -1031,11 +1050,16 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {  // 4 rows x 128 bytes per store
                             const int row = 4 * k + (lane >> 3);
-                            *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 7);
+                            if (row < live_rows)
+                                *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 7);
                         }
                         __syncwarp();
                     }
-                    if (rank == 0) p.ws_lse[c.slot * HEADS + h] = (m_used + __log2f(l)) * LN2;
+                    const float lse_v = (m_used + __log2f(l)) * LN2;
+                    if (rank == 0) {
+                        if (!direct) p.ws_lse[c.slot * HEADS + h] = lse_v;
+                        else if (lane < live_rows) p.lse[qrow0 + lane] = lse_v;
+                    }
                 }
                 if (rank == 0 && h == 0 && c.g_first == my_g)
                     p.ws_unit[c.u] = make_int2((int)c.g_first, c.g_last);
@@ -1134,9 +1158,15 @@ decode_combine_kernel(const Params p) {
     const Unit un = unit_of(pv, u);
     const int64_t qrow = (int64_t)bt * p.H + head;
     __nv_bfloat16* dst = p.o + qrow * DC + 16 * lane;
+    float* dst32 = p.o32 + qrow * DC + 16 * lane;
     if (un.pages == 0) {
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(0u, 0u, 0u, 0u);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(0u, 0u, 0u, 0u);
+        if (p.o32) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) reinterpret_cast<float4*>(dst32)[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        } else {
+            reinterpret_cast<uint4*>(dst)[0] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(dst)[1] = make_uint4(0u, 0u, 0u, 0u);
+        }
         if (lane == 0) p.lse[qrow] = -INFINITY;
         return;
     }
@@ -1188,10 +1218,16 @@ decode_combine_kernel(const Params p) {
             acc[4 * v + 3] = fmaf(wk, y.w, acc[4 * v + 3]);
         }
     }
-    reinterpret_cast<uint4*>(dst)[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                                                  pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-    reinterpret_cast<uint4*>(dst)[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
-                                                  pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+    if (p.o32) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+            reinterpret_cast<float4*>(dst32)[v] = make_float4(acc[4 * v], acc[4 * v + 1], acc[4 * v + 2], acc[4 * v + 3]);
+    } else {
+        reinterpret_cast<uint4*>(dst)[0] = make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                                                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+        reinterpret_cast<uint4*>(dst)[1] = make_uint4(pack_bf16x2(acc[8], acc[9]), pack_bf16x2(acc[10], acc[11]),
+                                                      pack_bf16x2(acc[12], acc[13]), pack_bf16x2(acc[14], acc[15]));
+    }
     if (lane == 0) p.lse[qrow] = L;
 }
 

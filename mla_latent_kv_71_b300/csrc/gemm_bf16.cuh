@@ -68,7 +68,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
     // bars[0..S): full, bars[S..2S): empty, bars[2S]: accumulator ready
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
-    int* flag = reinterpret_cast<int*>(tmem_slot + 1);
+    int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] skip, [2] reduce
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int m_tile = blockIdx.x;
@@ -119,10 +119,10 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
             }
             tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? z : 0, n0, pol);
         }
-        if (!ok) {  // let every issued copy land before the CTA can exit
-            for (int i = max(0, it - S); i < it; ++i)
-                mbar_wait(full0 + 8 * (i % S), (i / S) & 1, 0x102);
-        }
+        // every issued copy lands before the CTA can exit (on the normal path
+        // these phases have completed; after an abort they may not have)
+        for (int i = max(0, it - S); i < it; ++i)
+            mbar_wait_teardown(full0 + 8 * (i % S), (i / S) & 1, MLA_WAIT_LIMIT_NS);
     } else if (!skip && warp == 1 && lane == 0) {
         // --------------------------------------------------------------- MMA
         const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
@@ -149,70 +149,81 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     if (!ok) atomicExch(flag, 1);
 
     // ------------------------------------------------------------- epilogue
+    // good: this CTA's accumulator is complete and no error is known
+    bool good = false;
     if (!skip) {
-        const bool acc_ok = __syncthreads_and(mbar_wait(acc_bar, 0, 0x104) ? 1 : 0) != 0;
+        good = __syncthreads_and(mbar_wait(acc_bar, 0, 0x104) ? 1 : 0) != 0;
         tc_fence_after();
-        if (acc_ok && *flag == 0) {
-            const int m = m0 + warp * 32 + lane;
-            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-            const int n_valid = min(p.BN, p.N - n0);
-            if (p.splits == 1) {
-                __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
-                for (int c0 = 0; c0 < p.BN; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(trow + c0, r);
+        good = good && *flag == 0;
+    }
+    const int m = m0 + warp * 32 + lane;
+    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+    const int n_valid = min(p.BN, p.N - n0);
+    if (p.splits == 1) {
+        if (good) {
+            __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
+            for (int c0 = 0; c0 < p.BN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(trow + c0, r);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c0 + j < n_valid)
-                            dst[(int64_t)(n0 + c0 + j) * p.ldo] =
-                                __float2bfloat16_rn(__uint_as_float(r[j]));
-                }
-            } else {
-                const int Z = gridDim.y / p.n_tiles;
-                float* part = p.ws_part + (((int64_t)split * Z + z) * p.N) * p.M + m;
-                for (int c0 = 0; c0 < p.BN; c0 += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(trow + c0, r);
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < n_valid)
+                        dst[(int64_t)(n0 + c0 + j) * p.ldo] = __float2bfloat16_rn(__uint_as_float(r[j]));
+            }
+        }
+    } else {
+        const int Z = gridDim.y / p.n_tiles;
+        if (good) {
+            float* part = p.ws_part + (((int64_t)split * Z + z) * p.N) * p.M + m;
+            for (int c0 = 0; c0 < p.BN; c0 += 16) {
+                uint32_t r[16];
+                tmem_ld16(trow + c0, r);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c0 + j < n_valid)
-                            part[(int64_t)(n0 + c0 + j) * p.M] = __uint_as_float(r[j]);
-                }
-                __threadfence();
-                __syncthreads();
-                const int tile = (z * p.n_tiles + n_tile) * (p.M / BM) + m_tile;
-                if (threadIdx.x == 0) {
-                    const int prev = atomicAdd(p.ws_count + tile, 1);
-                    *flag = (prev == p.splits - 1) ? 2 : 0;
-                }
-                __syncthreads();
-                if (*flag == 2) {  // last split of this tile: reduce in split order
-                    __threadfence();
-                    __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
-                    // 8 columns at a time, each split's 8 loads issued together
-                    // (the sum still runs over the splits in order)
-                    for (int nb = 0; nb < n_valid; nb += 8) {
-                        float acc[8];
+                for (int j = 0; j < 16; ++j)
+                    if (c0 + j < n_valid) part[(int64_t)(n0 + c0 + j) * p.M] = __uint_as_float(r[j]);
+            }
+            __threadfence();
+        }
+        // Every CTA of the tile arrives on its counter -- also one that
+        // skipped or gave up -- and the last arrival resets it, so the
+        // counters are back at zero for the next call whatever happened in
+        // this one.  Only a last arrival that sees no error anywhere reduces.
+        __syncthreads();
+        const int tile = (z * p.n_tiles + n_tile) * (p.M / BM) + m_tile;
+        if (threadIdx.x == 0) {
+            const int prev = atomicAdd(p.ws_count + tile, 1);
+            const bool last = prev == p.splits - 1;
+            if (last) p.ws_count[tile] = 0;
+            flag[2] = last && good && !device_status_raised() ? 2 : 0;
+        }
+        __syncthreads();
+        if (flag[2] == 2) {  // last split of this tile: reduce in split order
+            __threadfence();
+            __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
+            // 8 columns at a time, each split's 8 loads issued together (the
+            // sum still runs over the splits in order)
+            for (int nb = 0; nb < n_valid; nb += 8) {
+                float acc[8];
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+                for (int j = 0; j < 8; ++j) acc[j] = 0.f;
 #pragma unroll 4
-                        for (int s = 0; s < p.splits; ++s) {
-                            const float* src = p.ws_part + (((int64_t)s * Z + z) * p.N + n0 + nb) * p.M + m;
-                            float v[8];
+                for (int s = 0; s < p.splits; ++s) {
+                    const float* src = p.ws_part + (((int64_t)s * Z + z) * p.N + n0 + nb) * p.M + m;
+                    float v[8];
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) v[j] = nb + j < n_valid ? __ldcg(src + (int64_t)j * p.M) : 0.f;
+                    for (int j = 0; j < 8; ++j) v[j] = nb + j < n_valid ? __ldcg(src + (int64_t)j * p.M) : 0.f;
 #pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[j] += v[j];
-                        }
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (nb + j < n_valid) dst[(int64_t)(n0 + nb + j) * p.ldo] = __float2bfloat16_rn(acc[j]);
-                    }
-                    if (threadIdx.x == 0) p.ws_count[tile] = 0;
+                    for (int j = 0; j < 8; ++j) acc[j] += v[j];
                 }
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (nb + j < n_valid) dst[(int64_t)(n0 + nb + j) * p.ldo] = __float2bfloat16_rn(acc[j]);
             }
         }
     }
+    // the products (and their commits) are done before TMEM goes away, even
+    // when the epilogue gave up waiting for them
+    if (!skip && threadIdx.x == 32) mbar_wait_teardown(acc_bar, 0, MLA_WAIT_LIMIT_NS);
     tc_fence_before();
     __syncthreads();
     if (warp == 1) tmem_dealloc(tmem, tmem_cols);

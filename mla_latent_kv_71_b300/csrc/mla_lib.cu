@@ -297,6 +297,13 @@ mla_status_t mla_get_device_status(mla_stream_t stream, uint32_t* detail) {
     }
 }
 
+mla_status_t mla_set_wait_limit(uint64_t ns) {
+    const uint64_t v = ns == 0 ? mla::MLA_WAIT_LIMIT_NS : ns;
+    if (cudaMemcpyToSymbol(mla::g_wait_limit_ns, &v, sizeof v) != cudaSuccess) return MLA_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MLA_ERR_CUDA;
+    return MLA_OK;
+}
+
 // ------------------------------------------------------------ mla_absorb_q
 
 mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int rows, int H,
@@ -660,12 +667,18 @@ int64_t mla_decode_plan(const int32_t* seq_lens_host, int B, int T, int H, int m
     return n;
 }
 
-mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv_pool,
-                             const int32_t* page_table, const int32_t* seq_lens,
-                             const int32_t* seq_lens_host, int B, int T, int H, int d_c,
-                             int d_r, int page_size, int max_pages, int64_t num_pages,
-                             float scale, int causal, void* o, float* lse, void* workspace,
-                             size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// mla_decode_attn (o in the input type) and mla_decode_attn_partial (o in
+// fp32 whatever the input type) share everything but the output type.
+mla_status_t decode_impl(const void* q_lat, const void* q_pe, const void* kv_pool,
+                         const int32_t* page_table, const int32_t* seq_lens,
+                         const int32_t* seq_lens_host, int B, int T, int H, int d_c, int d_r,
+                         int page_size, int max_pages, int64_t num_pages, float scale, int causal,
+                         void* o, bool o_f32, float* lse, void* workspace, size_t workspace_bytes,
+                         mla_dtype_t dtype, mla_stream_t stream) {
     if (!q_lat || !q_pe || !kv_pool || !page_table || !seq_lens || !o || !lse)
         return MLA_ERR_INVALID_ARG;
     if (B < 1 || T < 1 || H < 1 || d_c < 1 || d_r < 0 || page_size < 1 || max_pages < 1 ||
@@ -712,7 +725,8 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
     p.page_table = page_table;
     p.seq_lens = seq_lens;
-    p.o = static_cast<__nv_bfloat16*>(o);
+    p.o = o_f32 ? nullptr : static_cast<__nv_bfloat16*>(o);
+    p.o32 = o_f32 ? static_cast<float*>(o) : nullptr;
     p.lse = lse;
     char* ws = static_cast<char*>(workspace);
     p.ws_unit = reinterpret_cast<int2*>(ws + wl.unit_off);
@@ -750,6 +764,33 @@ mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv
     return launch_status();
 }
 
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_attn(const void* q_lat, const void* q_pe, const void* kv_pool,
+                             const int32_t* page_table, const int32_t* seq_lens,
+                             const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                             int d_r, int page_size, int max_pages, int64_t num_pages,
+                             float scale, int causal, void* o, float* lse, void* workspace,
+                             size_t workspace_bytes, mla_dtype_t dtype, mla_stream_t stream) {
+    return decode_impl(q_lat, q_pe, kv_pool, page_table, seq_lens, seq_lens_host, B, T, H, d_c, d_r,
+                       page_size, max_pages, num_pages, scale, causal, o, false, lse, workspace,
+                       workspace_bytes, dtype, stream);
+}
+
+mla_status_t mla_decode_attn_partial(const void* q_lat, const void* q_pe, const void* kv_pool,
+                                     const int32_t* page_table, const int32_t* seq_lens,
+                                     const int32_t* seq_lens_host, int B, int T, int H, int d_c,
+                                     int d_r, int page_size, int max_pages, int64_t num_pages,
+                                     float scale, int causal, float* o, float* lse,
+                                     void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                                     mla_stream_t stream) {
+    return decode_impl(q_lat, q_pe, kv_pool, page_table, seq_lens, seq_lens_host, B, T, H, d_c, d_r,
+                       page_size, max_pages, num_pages, scale, causal, o, dtype == MLA_BF16, lse,
+                       workspace, workspace_bytes, dtype, stream);
+}
+
 // ----------------------------------------------- mla_decode_attn_noalloc
 
 }  // extern "C"
@@ -759,29 +800,70 @@ namespace {
 // Scratch for mla_decode_attn_noalloc: a fixed array in device memory that
 // the CUDA runtime sets aside on every GPU that loads this library, for as
 // long as the process lives.  Calls share it and it keeps the last call's
-// contents (the decode scratch needs no initial value).
-constexpr size_t kNoallocScratchBytes = size_t(48) << 20;
+// contents (the decode scratch needs no initial value).  64 MiB holds the
+// decode scratch of up to 255 - (co-resident clusters) work units (sequence
+// x query token x 128-head group) -- 181 on a 148-SM B300, e.g. B = 128
+// sequences of one token and 128 heads.
+constexpr size_t kNoallocScratchBytes = size_t(64) << 20;
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoallocScratchBytes];
 
-// Device address of g_decode_scratch on each device, looked up once per
-// device (with that device current).  In host code the array's name is only
-// a stand-in for the symbol, never a device address.
-void* g_scratch_addr[kMaxDevices] = {};
+// Device address of g_decode_scratch, looked up with the device current and
+// cached per device together with the unique id of the CUDA context it was
+// looked up in.  A context created later on the same device (after
+// cudaDeviceReset, say) has another id, so its first call looks the address
+// up again instead of reusing a stale one.  In host code the array's name is
+// only a stand-in for the symbol, never a device address.
+struct ScratchAddr {
+    bool valid = false;
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];
 std::mutex g_scratch_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current context (false when there is
+// none, or the driver does not offer the query).
+bool current_context_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 void* decode_scratch_address() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) {
-            cudaGetLastError();
-            return nullptr;
-        }
-        g_scratch_addr[dev] = ptr;
+    ScratchAddr& e = g_scratch_addr[dev];
+    unsigned long long id = 0;
+    bool have_id = current_context_id(&id);
+    if (have_id && e.valid && e.ctx_id == id) return e.addr;
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_decode_scratch) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
     }
-    return g_scratch_addr[dev];
+    if (!have_id) have_id = current_context_id(&id);  // the lookup made the context current
+    e.valid = have_id;  // without a context id the address is looked up on every call
+    e.ctx_id = id;
+    e.addr = ptr;
+    return ptr;
 }
 
 }  // namespace

@@ -79,6 +79,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that suspends the thread for at most `hint_ns` (instead of the
+// hardware's own time slice) before it reports "not yet".
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Acquire at cluster scope: for data another CTA of the cluster wrote.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -93,29 +119,43 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // Bounded wait for the phase with the given parity.  `where` is recorded in
-// the status word's detail field when the wait gives up.  The status word
-// (another CTA gave up) and the clock are only looked at every 16th retry:
-// the status word is a global load, and a phase that completes while the
-// thread waits for it is only seen after it returns.
+// the status word's detail field when the wait gives up (after
+// wait_limit_ns(), 2 s unless the host shortened it).  try_wait suspends the
+// thread for a time slice of the hardware's choosing before it reports "not
+// yet"; when the host has set a limit below 1 ms (to test this path), each
+// try_wait is told to suspend for at most that limit, so that the wait can
+// give up on time (an explicit hint on every wait measurably slows the
+// normal path, so the default keeps the hardware's slice).  The clock is
+// read after every "not yet"; the status word (another CTA gave up), a
+// global load, after every 16th.
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_try_wait_any(uint32_t bar, uint32_t parity, bool hinted, uint32_t hint) {
+    if (hinted)
+        return kCluster ? mbar_try_wait_cluster_hint(bar, parity, hint) : mbar_try_wait_hint(bar, parity, hint);
+    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+}
+
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t where) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    const uint64_t limit = wait_limit_ns();
+    const bool hinted = limit < 1000000ull;
+    const uint32_t hint = (uint32_t)limit;
+    if (mbar_try_wait_any<kCluster>(bar, parity, hinted, hint)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
-        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
-            return true;
-        if ((n & 15u) == 0u) {
-            if (device_status_raised()) return false;
-            if (global_timer_ns() - t0 > MLA_WAIT_LIMIT_NS) {
-                raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
-                return false;
-            }
+        if (mbar_try_wait_any<kCluster>(bar, parity, hinted, hint)) return true;
+        if ((n & 15u) == 0u && device_status_raised()) return false;
+        if (global_timer_ns() - t0 > limit) {
+            raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
+            return false;
         }
     }
 }
 
-// Wait with its own time limit that ignores the device status word (used on
-// teardown paths, to let copies already in flight land before the CTA exits).
+// Wait with its own time limit that ignores the device status word and the
+// host's wait limit: used on teardown paths, for operations this CTA has
+// issued itself (TMA copies, tensor-core products), so that they land before
+// its shared memory or TMEM goes away.
 __device__ __forceinline__ bool mbar_wait_teardown(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = global_timer_ns();
     while (!mbar_try_wait_cluster(bar, parity))
@@ -400,6 +440,12 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// The two bf16 halves of a packed pair, widened exactly to an f32x2 pair
+// (a bf16 value is the high half of the fp32 with the same value).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t v) {
+    return (static_cast<uint64_t>(v & 0xFFFF0000u) << 32) | static_cast<uint64_t>(v << 16);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

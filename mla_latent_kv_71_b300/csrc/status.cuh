@@ -18,11 +18,19 @@ enum : uint32_t {
     MLA_DEV_BOUNDS = 2,
 };
 
-// A bounded wait gives up after this much wall time (globaltimer, ns).
+// A bounded wait gives up after this much wall time (globaltimer, ns) by
+// default.  The limit in use is g_wait_limit_ns, which the host may shorten
+// (mla_set_wait_limit) to exercise the failure path; teardown waits for
+// copies already in flight keep their own fixed limits.
 constexpr uint64_t MLA_WAIT_LIMIT_NS = 2000000000ull;
 
 // Defined once: the library is a single translation unit (mla_lib.cu).
 __device__ uint32_t g_device_status = 0u;
+// In constant memory: every wait reads it, and a constant-cache read costs
+// next to nothing (the host changes it only between calls).
+__constant__ uint64_t g_wait_limit_ns = MLA_WAIT_LIMIT_NS;
+
+__device__ __forceinline__ uint64_t wait_limit_ns() { return g_wait_limit_ns; }
 
 __device__ __forceinline__ bool device_status_raised() {
     return *reinterpret_cast<volatile uint32_t*>(&g_device_status) != 0u;

@@ -28,7 +28,7 @@ SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_
            "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes",
            "mla_cache_append_workspace_size", "mla_cache_append", "mla_project_q_workspace_size",
            "mla_project_q", "mla_fold_out_weights", "mla_out_proj_merged_workspace_size",
-           "mla_out_proj_merged"]
+           "mla_out_proj_merged", "mla_set_wait_limit", "mla_decode_attn_partial"]
 
 
 class MLAError(RuntimeError):
@@ -95,6 +95,10 @@ def _lib():
         lib.mla_out_proj_merged_workspace_size.restype = Z
         lib.mla_out_proj_merged.argtypes = [P, P, P, I, I, I, I, P, Z, I, P]
         lib.mla_out_proj_merged.restype = I
+        lib.mla_decode_attn_partial.argtypes = lib.mla_decode_attn.argtypes
+        lib.mla_decode_attn_partial.restype = I
+        lib.mla_set_wait_limit.argtypes = [ctypes.c_uint64]
+        lib.mla_set_wait_limit.restype = I
         _LIB = lib
     return _LIB
 
@@ -172,6 +176,37 @@ def decode_attn(q_lat, q_pe, kv_pool, page_table, seq_lens, scale: float, causal
         host = ctypes.c_void_p(seq_lens_host.data_ptr())
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check("mla_decode_attn", _lib().mla_decode_attn(
+        _ptr(q_lat), _ptr(q_pe), _ptr(kv_pool), _ptr(page_table), _ptr(seq_lens), host, B, T, H,
+        d_c, d_r, page, max_pages, num_pages, float(scale), int(bool(causal)), _ptr(o), _ptr(lse),
+        _ptr(workspace), ws_bytes, dt, _stream(stream)))
+    return o, lse
+
+
+def decode_attn_partial(q_lat, q_pe, kv_pool, page_table, seq_lens, scale: float,
+                        causal: bool = False, o=None, lse=None, workspace=None,
+                        seq_lens_host=None, stream=None):
+    """decode_attn with o in fp32 (a part's normalised result, for merging
+    with other parts by combine_splits); returns (o fp32, lse)."""
+    B, T, H, d_c = q_lat.shape
+    d_r = q_pe.shape[3]
+    num_pages, page, width = kv_pool.shape
+    max_pages = page_table.shape[1]
+    if o is None:
+        o = torch.empty((B, T, H, d_c), dtype=torch.float32, device=q_lat.device)
+    if lse is None:
+        lse = torch.empty((B, T, H), dtype=torch.float32, device=q_lat.device)
+    if o.dtype != torch.float32:
+        raise TypeError("decode_attn_partial writes an fp32 o")
+    dt = _dt(q_lat)
+    need = int(_lib().mla_decode_workspace_size(B, T, H, d_c, dt))
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q_lat.device)
+    host = None
+    if seq_lens_host is not None:
+        seq_lens_host = seq_lens_host.to(torch.int32).contiguous()
+        host = ctypes.c_void_p(seq_lens_host.data_ptr())
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_decode_attn_partial", _lib().mla_decode_attn_partial(
         _ptr(q_lat), _ptr(q_pe), _ptr(kv_pool), _ptr(page_table), _ptr(seq_lens), host, B, T, H,
         d_c, d_r, page, max_pages, num_pages, float(scale), int(bool(causal)), _ptr(o), _ptr(lse),
         _ptr(workspace), ws_bytes, dt, _stream(stream)))
@@ -332,6 +367,12 @@ def get_device_status(stream=None) -> tuple[int, int]:
     detail = ctypes.c_uint32(0)
     code = _lib().mla_get_device_status(_stream(stream), ctypes.byref(detail))
     return int(code), int(detail.value)
+
+
+def set_wait_limit(ns: int) -> None:
+    """How long the library's kernels wait for a pipeline step before giving
+    up with MLA_ERR_TIMEOUT (ns; 0 restores the default of 2 s)."""
+    _check("mla_set_wait_limit", _lib().mla_set_wait_limit(int(ns)))
 
 
 def set_decode_events(start: torch.cuda.Event | None, end: torch.cuda.Event | None) -> None:
