@@ -79,32 +79,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// try_wait that suspends the thread for at most `hint_ns` (instead of the
-// hardware's own time slice) before it reports "not yet".
-__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_try_wait_cluster_hint(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Acquire at cluster scope: for data another CTA of the cluster wrote.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -122,32 +96,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 // the status word's detail field when the wait gives up (after
 // wait_limit_ns(), 2 s unless the host shortened it).  try_wait suspends the
 // thread for a time slice of the hardware's choosing before it reports "not
-// yet"; when the host has set a limit below 1 ms (to test this path), each
-// try_wait is told to suspend for at most that limit, so that the wait can
-// give up on time (an explicit hint on every wait measurably slows the
-// normal path, so the default keeps the hardware's slice).  The clock is
-// read after every "not yet"; the status word (another CTA gave up), a
-// global load, after every 16th.
-template <bool kCluster = false>
-__device__ __forceinline__ bool mbar_try_wait_any(uint32_t bar, uint32_t parity, bool hinted, uint32_t hint) {
-    if (hinted)
-        return kCluster ? mbar_try_wait_cluster_hint(bar, parity, hint) : mbar_try_wait_hint(bar, parity, hint);
-    return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-}
-
+// yet"; the clock and the status word (another CTA gave up; a global load)
+// are looked at after every 16th "not yet", or after every one when the host
+// has set a limit below 1 ms (to test this path), so that such a wait gives
+// up on time.  (Reading the clock after every retry on the normal path, or
+// a hinted try_wait, measurably slows the attention kernel.)
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t where) {
+    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t limit = wait_limit_ns();
-    const bool hinted = limit < 1000000ull;
-    const uint32_t hint = (uint32_t)limit;
-    if (mbar_try_wait_any<kCluster>(bar, parity, hinted, hint)) return true;
+    const uint32_t every = limit < 1000000ull ? 0u : 15u;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t n = 1;; ++n) {
-        if (mbar_try_wait_any<kCluster>(bar, parity, hinted, hint)) return true;
-        if ((n & 15u) == 0u && device_status_raised()) return false;
-        if (global_timer_ns() - t0 > limit) {
-            raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
-            return false;
+        if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+            return true;
+        if ((n & every) == 0u) {
+            if (device_status_raised()) return false;
+            if (global_timer_ns() - t0 > limit) {
+                raise_device_status(MLA_DEV_TIMEOUT, (where & 0xFFFu) | ((blockIdx.x & 0xFFFu) << 12));
+                return false;
+            }
         }
     }
 }

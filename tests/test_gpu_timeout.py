@@ -4,9 +4,9 @@ Every wait of a pipeline step in the library's kernels gives up after a
 limit, raises MLA_ERR_TIMEOUT in the device status word and lets the kernel
 wind down: the CTA waits for the copies and tensor-core products it issued
 itself, frees its TMEM and exits.  These tests shorten the limit from the
-host to 1 ns, so that the first wait that is not met at once gives up, and
-check that the call reports the timeout and that the next call on the same
-context computes the right result.  Nothing is broken on purpose: no
+host to 1 ns, so that a wait still open after the hardware's first
+suspension gives up, and check that the call reports the timeout and that
+the next call on the same context computes the right result.  Nothing is broken on purpose: no
 arrival is skipped and no input is invalid; the waits simply give up early.
 """
 
@@ -34,16 +34,24 @@ def _cuda():
     mla.set_wait_limit(0)
 
 
-def _timed_out(fn):
-    """Run fn with a 1 ns wait limit; returns (status code, detail)."""
-    mla.get_device_status()
-    mla.set_wait_limit(1)
-    try:
-        fn()
-        torch.cuda.synchronize()
-        return mla.get_device_status()
-    finally:
-        mla.set_wait_limit(0)
+def _timed_out(fn, tries=3):
+    """Run fn with a 1 ns wait limit until a call reports the timeout (at
+    most `tries` calls); returns the last (status code, detail).  A wait
+    only gives up when the hardware's first suspension inside try_wait ends
+    before the phase completes, so a single call may see every wait met."""
+    code, detail = 0, 0
+    for _ in range(tries):
+        mla.get_device_status()
+        mla.set_wait_limit(1)
+        try:
+            fn()
+            torch.cuda.synchronize()
+            code, detail = mla.get_device_status()
+        finally:
+            mla.set_wait_limit(0)
+        if code != 0:
+            break
+    return code, detail
 
 
 def test_decode_wait_gives_up_and_the_next_call_is_correct():
