@@ -23,6 +23,8 @@ Parity status of each function (what pins it is listed in the tests):
                                 the weights
   project, naive_decode ....... pinned by a library routine (SDPA) and the
                                 identity against the absorbed route
+  naive_prefill ............... pinned by naive_decode with T = L and by a
+                                library routine (causal SDPA)
 """
 
 from __future__ import annotations
@@ -82,6 +84,8 @@ def _declare(lib):
     lib.orc_absorb_q.argtypes = [_P, _I, _P, _I, _I, _I, _I, _I, _P]
     lib.orc_decode_attn.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                     _I, _I, _D, _I, _P, _L, _P, _P]
+    lib.orc_naive_prefill.argtypes = [_P, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I,
+                                      _I, _D, _I, _P, _L, _P, _P]
     lib.orc_weight_spread.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _D, _I, _P, _L, _P]
     lib.orc_attention_weights.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I,
@@ -330,3 +334,36 @@ def naive_decode(cache, q_nope, q_pe, w_uk, w_uv, w_o, L, scale, causal=False, l
                          dwv, wo_p, dwo, B, T, L, H, d_h, d_c, d_r, d, float(scale),
                          int(bool(causal)), _ptr(u), out_p)
     return u, out
+
+
+def naive_prefill(cache, q_nope, q_pe, w_uk, w_uv, scale, causal=True, sel=None, lib=None):
+    """Training-form attention with every token a query.
+
+    cache [B, L, d_c+d_r] rows [c ; k^R]; q_nope [B,L,H,d_h], q_pe [B,L,H,d_r];
+    w_uk / w_uv [H,d_h,d_c].  Returns (u [B,L,H,d_h], lse [B,L,H]) float64, or
+    with sel (flattened (b*L + t)*H + i rows) (u [n,d_h], lse [n]).
+    """
+    lib = lib or load()
+    cc = np.ascontiguousarray(cache, dtype=np.float64)
+    B, L = cc.shape[0], cc.shape[1]
+    cc = cc.reshape(B * L, -1)
+    qn, dqn = _arr(q_nope)
+    qp, dqp = _arr(q_pe)
+    wk, dwk = _arr(w_uk)
+    wv, dwv = _arr(w_uv)
+    H, d_h = qn.shape[2], qn.shape[3]
+    d_r = qp.shape[3]
+    d_c = wk.shape[2]
+    if sel is None:
+        n, sel_arr = B * L * H, None
+    else:
+        sel_arr = np.ascontiguousarray(sel, dtype=np.int64)
+        n = sel_arr.shape[0]
+    u = np.empty((n, d_h), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    lib.orc_naive_prefill(_ptr(cc), _ptr(qn), dqn, _ptr(qp), dqp, _ptr(wk), dwk, _ptr(wv), dwv,
+                          B, L, H, d_h, d_c, d_r, float(scale), int(bool(causal)),
+                          _ptr(sel_arr) if sel_arr is not None else None, n, _ptr(u), _ptr(lse))
+    if sel is None:
+        return u.reshape(B, L, H, d_h), lse.reshape(B, L, H)
+    return u, lse

@@ -221,6 +221,87 @@ void orc_decode_attn(const void* q_lat, int dql, const void* q_pe, int dqp,
 }
 
 /*
+ * Training-form (unabsorbed) attention over whole sequences, every cached
+ * token a query ([Mishra] "Multi-head Latent Attention": the unabsorbed form
+ * is the one used in training; [llms] "Low-Rank Key-Value Joint
+ * Compression" and "The Positional Problem and Decoupled RoPE" for the
+ * definitions).  For sequence b, query position t and head i:
+ *   k_{j,i} = [W^UK_i c_j ; k^R_j],  v_{j,i} = W^UV_i c_j
+ *   s_j     = q_{t,i} . k_{j,i} * scale,   j <= t when causal, else all j < L
+ *   u_{t,i} = sum_j softmax_j(s) v_{j,i},  lse_{t,i} = ln sum_j e^{s_j}
+ * The same definitions as orc_naive_decode with T = L; the keys and values
+ * of a sequence (they do not depend on the query) are expanded once.
+ * cache [B*L, d_c+d_r] rows [c ; k^R]; q_nope [B,L,H,d_h]; q_pe [B,L,H,d_r];
+ * sel lists flattened (b*L + t)*H + i rows (NULL: all), outputs compact in
+ * selection order: u [rows, d_h], lse [rows].
+ */
+void orc_naive_prefill(const double* cache, const void* q_nope, int dqn,
+                       const void* q_pe, int dqp, const void* w_uk, int dwk,
+                       const void* w_uv, int dwv, int B, int L, int H, int d_h,
+                       int d_c, int d_r, double scale, int causal,
+                       const int64_t* sel, int64_t n_sel, double* u, double* lse) {
+    int64_t width = (int64_t)d_c + d_r;
+    int64_t kw = (int64_t)d_h + d_r;
+    int64_t total = sel ? n_sel : (int64_t)B * L * H;
+    /* expanded keys and values of every (b, j, i): [B, L, H, d_h + d_r], [B, L, H, d_h] */
+    double* K = (double*)malloc(sizeof(double) * (size_t)B * L * H * kw);
+    double* V = (double*)malloc(sizeof(double) * (size_t)B * L * H * d_h);
+    #pragma omp parallel for collapse(3) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int j = 0; j < L; ++j)
+            for (int i = 0; i < H; ++i) {
+                const double* row = cache + ((int64_t)b * L + j) * width;
+                double* k = K + (((int64_t)b * L + j) * H + i) * kw;
+                double* v = V + (((int64_t)b * L + j) * H + i) * d_h;
+                for (int e = 0; e < d_h; ++e) {
+                    double kx = 0.0, vx = 0.0;  /* (W^UK_i c_j)[e], (W^UV_i c_j)[e] */
+                    int64_t wr = ((int64_t)i * d_h + e) * d_c;
+                    for (int c = 0; c < d_c; ++c) {
+                        kx += rd(w_uk, dwk, wr + c) * row[c];
+                        vx += rd(w_uv, dwv, wr + c) * row[c];
+                    }
+                    k[e] = kx;
+                    v[e] = vx;
+                }
+                for (int e = 0; e < d_r; ++e) k[d_h + e] = row[d_c + e];
+            }
+    #pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)L);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < total; ++r) {
+            int64_t f = sel ? sel[r] : r;
+            int i = (int)(f % H);
+            int t = (int)((f / H) % L);
+            int b = (int)(f / ((int64_t)H * L));
+            int64_t n = causal ? (int64_t)t + 1 : L;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                const double* k = K + (((int64_t)b * L + j) * H + i) * kw;
+                double acc = 0.0;
+                for (int e = 0; e < d_h; ++e) acc += rd(q_nope, dqn, f * d_h + e) * k[e];
+                for (int e = 0; e < d_r; ++e) acc += rd(q_pe, dqp, f * d_r + e) * k[d_h + e];
+                s[j] = acc * scale;
+                if (s[j] > m) m = s[j];
+            }
+            double l = 0.0;
+            for (int64_t j = 0; j < n; ++j) l += exp(s[j] - m);
+            double* ur = u + r * d_h;
+            for (int e = 0; e < d_h; ++e) ur[e] = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                double a = exp(s[j] - m) / l;
+                const double* v = V + (((int64_t)b * L + j) * H + i) * d_h;
+                for (int e = 0; e < d_h; ++e) ur[e] += a * v[e];
+            }
+            lse[r] = m + log(l);
+        }
+        free(s);
+    }
+    free(K);
+    free(V);
+}
+
+/*
  * Sensitivity of o to rounding the attention weights (test infrastructure,
  * not a step of the method).  For every listed (b, t, i) and latent column c
  *     D[c] = sum_j a_j |c_j[c] - o[c]|

@@ -468,10 +468,48 @@ def pin_weight_spread(lib):
     assert np.abs(Ds).max() < 1e-13
 
 
+def pin_naive_prefill(lib):
+    """Training-form attention with every token a query: equal to the naive
+    route with T = L causal queries, and to torch's fp64 causal
+    scaled_dot_product_attention on keys and values expanded by matmul
+    ([Mishra] "Multi-head Latent Attention": the unabsorbed form); a
+    selection of rows equals those rows of the full result."""
+    g = torch.Generator().manual_seed(41)
+    B, L, H, d_h, d_c, d_r = 2, 37, 3, 8, 16, 4
+    cache = torch.randn((B, L, d_c + d_r), generator=g, dtype=torch.float64)
+    qn = torch.randn((B, L, H, d_h), generator=g, dtype=torch.float64)
+    qp = torch.randn((B, L, H, d_r), generator=g, dtype=torch.float64)
+    w_uk = torch.randn((H, d_h, d_c), generator=g, dtype=torch.float64) / 4
+    w_uv = torch.randn((H, d_h, d_c), generator=g, dtype=torch.float64) / 4
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    u, lse = oracle.naive_prefill(cache.numpy(), qn, qp, w_uk, w_uv, scale, causal=True, lib=lib)
+    u_dec, _ = oracle.naive_decode(cache.reshape(B * L, -1).numpy(), qn, qp, w_uk, w_uv, None, L,
+                                   scale, causal=True, lib=lib)
+    assert np.abs(u - u_dec).max() < 1e-12
+    c = cache[..., :d_c]
+    k = torch.cat([torch.einsum("blc,hec->bhle", c, w_uk),
+                   cache[..., d_c:].unsqueeze(1).expand(B, H, L, d_r)], -1)
+    v = torch.einsum("blc,hec->bhle", c, w_uv)
+    q = torch.cat([qn, qp], -1).permute(0, 2, 1, 3)
+    for causal in (True, False):
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+        got, lse_c = oracle.naive_prefill(cache.numpy(), qn, qp, w_uk, w_uv, scale, causal=causal,
+                                          lib=lib)
+        assert np.abs(got - ref.permute(0, 2, 1, 3).numpy()).max() < 1e-12
+        s = (q @ k.transpose(-1, -2)) * scale
+        if causal:
+            s = s.masked_fill(torch.ones(L, L, dtype=torch.bool).triu(1), float("-inf"))
+        assert np.abs(lse_c - torch.logsumexp(s, -1).permute(0, 2, 1).numpy()).max() < 1e-12
+    sel = np.array([0, 5, B * L * H - 1, 100])
+    us, ls = oracle.naive_prefill(cache.numpy(), qn, qp, w_uk, w_uv, scale, causal=True, sel=sel,
+                                  lib=lib)
+    assert np.array_equal(us, u.reshape(-1, d_h)[sel]) and np.array_equal(ls, lse.reshape(-1)[sel])
+
+
 ALL_PINS = [
     pin_cache_accounting, pin_absorption_cost, pin_rope, pin_naive_equals_absorbed,
     pin_naive_equals_absorbed_at_model_widths, pin_naive_vs_library_sdpa, pin_project_vs_library, pin_position_shift_invariance,
     pin_decode_vs_library_sdpa, pin_decode_closed_forms, pin_softmax_rows_sum_to_one,
     pin_fp64_rounding_is_negligible, pin_page_permutation_invariance, pin_combine_split_identity, pin_empty_sequence,
-    pin_out_proj_vs_library, pin_bf16_widening, pin_weight_spread,
+    pin_out_proj_vs_library, pin_bf16_widening, pin_weight_spread, pin_naive_prefill,
 ]

@@ -55,6 +55,10 @@ MUTANTS = {
                            "dst[c] += a[j] * (rd(pool, dp, row + c) - o[c]);"),
     "spread_about_zero": ("dst[c] += a[j] * fabs(rd(pool, dp, row + c) - o[c]);",
                           "dst[c] += a[j] * fabs(rd(pool, dp, row + c));"),
+    "prefill_causal_off_by_one": ("int64_t n = causal ? (int64_t)t + 1 : L;",
+                                  "int64_t n = causal ? (int64_t)t : L;"),
+    "prefill_value_uses_w_uk": ("vx += rd(w_uv, dwv, wr + c) * row[c];",
+                                "vx += rd(w_uk, dwk, wr + c) * row[c];"),
     "project_kr_uses_w_dkv": ("acc += rd(w_kr, dw2, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);",
                               "acc += rd(w_dkv, dw1, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);"),
 }
