@@ -25,6 +25,8 @@ Parity status of each function (what pins it is listed in the tests):
                                 identity against the absorbed route
   naive_prefill ............... pinned by naive_decode with T = L and by a
                                 library routine (causal SDPA)
+  prefill_attn ................ pinned by naive_prefill on exact expansions
+                                and by a library routine (causal SDPA)
 """
 
 from __future__ import annotations
@@ -86,6 +88,8 @@ def _declare(lib):
                                     _I, _I, _D, _I, _P, _L, _P, _P]
     lib.orc_naive_prefill.argtypes = [_P, _P, _I, _P, _I, _P, _I, _P, _I, _I, _I, _I, _I, _I,
                                       _I, _D, _I, _P, _L, _P, _P]
+    lib.orc_prefill_attn.argtypes = [_P, _I, _P, _I, _P, _I, _P, _I, _L, _L, _P, _I, _I, _I, _I,
+                                     _I, _I, _D, _I, _P, _L, _P, _P]
     lib.orc_weight_spread.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                                       _I, _I, _D, _I, _P, _L, _P]
     lib.orc_attention_weights.argtypes = [_P, _I, _P, _I, _P, _I, _P, _P, _I, _I, _I, _I,
@@ -366,4 +370,38 @@ def naive_prefill(cache, q_nope, q_pe, w_uk, w_uv, scale, causal=True, sel=None,
                           _ptr(sel_arr) if sel_arr is not None else None, n, _ptr(u), _ptr(lse))
     if sel is None:
         return u.reshape(B, L, H, d_h), lse.reshape(B, L, H)
+    return u, lse
+
+
+def prefill_attn(q_nope, q_pe, k_nope, k_pe, v, L, scale, causal=True, k_pe_off=0, sel=None,
+                 lib=None):
+    """Attention of given per-head keys and values, every token a query.
+
+    q_nope, k_nope, v [rows, H, d_h]; q_pe [rows, H, d_r]; k_pe [rows, w] with
+    the RoPE key in columns k_pe_off .. k_pe_off + d_r - 1 (cache rows work
+    as they are); rows = B * L.  Returns (u [rows, H, d_h], lse [rows, H])
+    float64, or with sel (flattened token * H + head rows) (u [n, d_h], lse [n]).
+    """
+    lib = lib or load()
+    qn, dqn = _arr(q_nope)
+    qp, dqp = _arr(q_pe)
+    kn, dkn = _arr(k_nope)
+    kp, dkp = _arr(k_pe)
+    vv, dv = _arr(v)
+    rows, H, d_h = qn.shape
+    d_r = qp.shape[2]
+    B = rows // L
+    if sel is None:
+        n, sel_arr = rows * H, None
+    else:
+        sel_arr = np.ascontiguousarray(sel, dtype=np.int64)
+        n = sel_arr.shape[0]
+    u = np.empty((n, d_h), dtype=np.float64)
+    lse = np.empty((n,), dtype=np.float64)
+    lib.orc_prefill_attn(_ptr(qn), dqn, _ptr(qp), dqp, _ptr(kn), dkn, _ptr(kp), dkp, kp.shape[1],
+                         int(k_pe_off), _ptr(vv), dv, B, L, H, d_h, d_r, float(scale),
+                         int(bool(causal)), _ptr(sel_arr) if sel_arr is not None else None, n,
+                         _ptr(u), _ptr(lse))
+    if sel is None:
+        return u.reshape(rows, H, d_h), lse.reshape(rows, H)
     return u, lse

@@ -302,6 +302,61 @@ void orc_naive_prefill(const double* cache, const void* q_nope, int dqn,
 }
 
 /*
+ * Softmax attention of given per-head keys and values, every token a query:
+ * the attention half of the training-form route above, on keys and values
+ * already expanded ([Mishra] "Multi-head Latent Attention"; [llms] "The
+ * Positional Problem and Decoupled RoPE": the RoPE key k^R_j is shared by
+ * all heads).  For sequence b, position t, head i:
+ *   s_j     = (q^C_{t,i} . k^C_{j,i} + q^R_{t,i} . k^R_j) * scale
+ *   u_{t,i} = sum_j softmax_j(s) v_{j,i},   lse_{t,i} = ln sum_j e^{s_j}
+ * over j <= t (causal) or all j < L.  q_nope, k_nope, v [B*L, H, d_h];
+ * q_pe [B*L, H, d_r]; k_pe rows of k_pe_ld values, the RoPE key from
+ * column k_pe_off (so that it can be read straight from cache rows).
+ * sel, u, lse as in orc_naive_prefill.
+ */
+void orc_prefill_attn(const void* q_nope, int dqn, const void* q_pe, int dqp,
+                      const void* k_nope, int dkn, const void* k_pe, int dkp,
+                      int64_t k_pe_ld, int64_t k_pe_off, const void* v, int dv,
+                      int B, int L, int H, int d_h, int d_r, double scale, int causal,
+                      const int64_t* sel, int64_t n_sel, double* u, double* lse) {
+    int64_t total = sel ? n_sel : (int64_t)B * L * H;
+    #pragma omp parallel
+    {
+        double* sc = (double*)malloc(sizeof(double) * (size_t)L);
+        #pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < total; ++r) {
+            int64_t f = sel ? sel[r] : r;
+            int i = (int)(f % H);
+            int64_t tok = f / H;               /* b * L + t */
+            int t = (int)(tok % L);
+            int64_t first = tok - t;           /* the sequence's first token */
+            int64_t n = causal ? t + (int64_t)1 : (int64_t)L;  /* visible keys */
+            double mx = -INFINITY;
+            for (int64_t j = 0; j < n; ++j) {
+                int64_t kr = (first + j) * H + i;
+                double acc = 0.0;
+                for (int e = 0; e < d_h; ++e) acc += rd(q_nope, dqn, f * d_h + e) * rd(k_nope, dkn, kr * d_h + e);
+                for (int e = 0; e < d_r; ++e)
+                    acc += rd(q_pe, dqp, f * d_r + e) * rd(k_pe, dkp, (first + j) * k_pe_ld + k_pe_off + e);
+                sc[j] = acc * scale;
+                if (sc[j] > mx) mx = sc[j];
+            }
+            double den = 0.0;
+            for (int64_t j = 0; j < n; ++j) den += exp(sc[j] - mx);
+            double* ur = u + r * d_h;
+            for (int e = 0; e < d_h; ++e) ur[e] = 0.0;
+            for (int64_t j = 0; j < n; ++j) {
+                double w = exp(sc[j] - mx) / den;
+                int64_t vr = (first + j) * H + i;
+                for (int e = 0; e < d_h; ++e) ur[e] += w * rd(v, dv, vr * d_h + e);
+            }
+            lse[r] = mx + log(den);
+        }
+        free(sc);
+    }
+}
+
+/*
  * Sensitivity of o to rounding the attention weights (test infrastructure,
  * not a step of the method).  For every listed (b, t, i) and latent column c
  *     D[c] = sum_j a_j |c_j[c] - o[c]|

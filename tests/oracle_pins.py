@@ -506,10 +506,44 @@ def pin_naive_prefill(lib):
     assert np.array_equal(us, u.reshape(-1, d_h)[sel]) and np.array_equal(ls, lse.reshape(-1)[sel])
 
 
+def pin_prefill_attn(lib):
+    """Attention of given keys and values equals the training-form route on
+    the exact expansions of the same cache (so it is the route's attention
+    half), and torch's fp64 causal scaled_dot_product_attention; the RoPE key
+    may be read from cache rows at a column offset."""
+    g = torch.Generator().manual_seed(43)
+    B, L, H, d_h, d_c, d_r = 2, 29, 3, 8, 16, 4
+    cache = torch.randn((B, L, d_c + d_r), generator=g, dtype=torch.float64)
+    qn = torch.randn((B * L, H, d_h), generator=g, dtype=torch.float64)
+    qp = torch.randn((B * L, H, d_r), generator=g, dtype=torch.float64)
+    w_uk = torch.randn((H, d_h, d_c), generator=g, dtype=torch.float64) / 4
+    w_uv = torch.randn((H, d_h, d_c), generator=g, dtype=torch.float64) / 4
+    scale = 1.0 / math.sqrt(d_h + d_r)
+    c = cache.reshape(B * L, -1)[:, :d_c]
+    kn = torch.einsum("rc,hec->rhe", c, w_uk)
+    vv = torch.einsum("rc,hec->rhe", c, w_uv)
+    rows = cache.reshape(B * L, -1)
+    u, lse = oracle.prefill_attn(qn, qp, kn, rows, vv, L, scale, causal=True, k_pe_off=d_c, lib=lib)
+    u_ref, lse_ref = oracle.naive_prefill(cache.numpy(), qn.reshape(B, L, H, d_h),
+                                          qp.reshape(B, L, H, d_r), w_uk, w_uv, scale, lib=lib)
+    assert np.abs(u - u_ref.reshape(u.shape)).max() < 1e-12
+    assert np.abs(lse - lse_ref.reshape(lse.shape)).max() < 1e-12
+    q = torch.cat([qn, qp], -1).reshape(B, L, H, -1).permute(0, 2, 1, 3)
+    k = torch.cat([kn, rows[:, d_c:].unsqueeze(1).expand(B * L, H, d_r)], -1)
+    k = k.reshape(B, L, H, -1).permute(0, 2, 1, 3)
+    v = vv.reshape(B, L, H, d_h).permute(0, 2, 1, 3)
+    for causal in (True, False):
+        ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=causal, scale=scale)
+        got, _ = oracle.prefill_attn(qn, qp, kn, rows, vv, L, scale, causal=causal, k_pe_off=d_c,
+                                     lib=lib)
+        assert np.abs(got - ref.permute(0, 2, 1, 3).reshape(B * L, H, d_h).numpy()).max() < 1e-12
+
+
 ALL_PINS = [
     pin_cache_accounting, pin_absorption_cost, pin_rope, pin_naive_equals_absorbed,
     pin_naive_equals_absorbed_at_model_widths, pin_naive_vs_library_sdpa, pin_project_vs_library, pin_position_shift_invariance,
     pin_decode_vs_library_sdpa, pin_decode_closed_forms, pin_softmax_rows_sum_to_one,
     pin_fp64_rounding_is_negligible, pin_page_permutation_invariance, pin_combine_split_identity, pin_empty_sequence,
     pin_out_proj_vs_library, pin_bf16_widening, pin_weight_spread, pin_naive_prefill,
+    pin_prefill_attn,
 ]

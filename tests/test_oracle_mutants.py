@@ -59,6 +59,12 @@ MUTANTS = {
                                   "int64_t n = causal ? (int64_t)t : L;"),
     "prefill_value_uses_w_uk": ("vx += rd(w_uv, dwv, wr + c) * row[c];",
                                 "vx += rd(w_uk, dwk, wr + c) * row[c];"),
+    "prefill_attn_rope_offset_ignored": (
+        "acc += rd(q_pe, dqp, f * d_r + e) * rd(k_pe, dkp, (first + j) * k_pe_ld + k_pe_off + e);",
+        "acc += rd(q_pe, dqp, f * d_r + e) * rd(k_pe, dkp, (first + j) * k_pe_ld + e);"),
+    "prefill_attn_ignores_causal": ("int64_t n = causal ? t + (int64_t)1 : (int64_t)L;",
+                                    "int64_t n = (int64_t)L + 0 * t;"),
+    "prefill_attn_value_row_of_query": ("int64_t vr = (first + j) * H + i;", "int64_t vr = f;"),
     "project_kr_uses_w_dkv": ("acc += rd(w_kr, dw2, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);",
                               "acc += rd(w_dkv, dw1, (int64_t)e * d + k) * rd(h, dh_t, hrow + k);"),
 }
