@@ -347,6 +347,55 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
                            mla_stream_t stream);
 
 /*
+ * Prefill in the training (unabsorbed) form ([Mishra] "Multi-head Latent
+ * Attention": the unabsorbed form is the one used in training; [llms]
+ * "Low-Rank Key-Value Joint Compression" for the up-projections and "The
+ * Positional Problem and Decoupled RoPE" for the shared RoPE key).  Every
+ * cached token of a sequence is a query; per query position t and head i
+ *     k_{j,i} = [W^UK_i c_j ; k^R_j],   v_{j,i} = W^UV_i c_j
+ *     u_{t,i} = sum_j softmax_j(q_{t,i} . k_{j,i} * scale) v_{j,i}
+ * over j <= t (causal) or all j, and out_t = W^O concat_i u_{t,i}.  With
+ * many queries this costs 2(d_h + d_r) + 2 d_h FLOPs per (query, key, head)
+ * against 2(d_c + d_r) + 2 d_c for the absorbed form, so prefill takes it.
+ * bf16 only (MLA_FP32 returns MLA_ERR_UNSUPPORTED).
+ *
+ * mla_prefill_expand -- the per-head keys and values of every cache row:
+ *   kv     [rows, d_c + d_r]  cache rows [c ; k^R] (contiguous, in token order)
+ *   w_uk, w_uv [H, d_h, d_c]
+ *   k_nope [rows, H, d_h]     output, W^UK_i c
+ *   v      [rows, H, d_h]     output, W^UV_i c
+ * H * d_h % 128 == 0, d_c % 64 == 0.
+ */
+mla_status_t mla_prefill_expand(const void* kv, const void* w_uk, const void* w_uv, void* k_nope,
+                                void* v, int rows, int H, int d_h, int d_c, int d_r,
+                                mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * mla_prefill_attn -- causal (or full) attention of B sequences of L tokens:
+ *   q_nope [B*L, H, d_h], q_pe [B*L, H, d_r]   queries (q^R already rotated)
+ *   k_nope, v [B*L, H, d_h]                    from mla_prefill_expand
+ *   kv     [B*L, d_c + d_r]                    cache rows; k^R is read from
+ *                                              columns d_c .. d_c + d_r - 1
+ *   u      [B*L, H, d_h]  output;  lse [B*L, H] fp32 output (natural log)
+ * d_h == 128, d_r == 64, d_c % 64 == 0, any L >= 1, H >= 1.
+ */
+mla_status_t mla_prefill_attn(const void* q_nope, const void* q_pe, const void* k_nope,
+                              const void* kv, const void* v, int B, int L, int H, int d_h, int d_c,
+                              int d_r, float scale, int causal, void* u, float* lse,
+                              mla_dtype_t dtype, mla_stream_t stream);
+
+/* Bytes of workspace mla_prefill_out needs (0 when none). */
+size_t mla_prefill_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t dtype);
+
+/*
+ * mla_prefill_out -- out [rows, d] = W^O u for u [rows, H * d_h] and
+ * W^O [d, H * d_h]; d % 128 == 0.  workspace >= mla_prefill_workspace_size.
+ */
+mla_status_t mla_prefill_out(const void* u, const void* w_o, void* out, int rows, int H, int d_h,
+                             int d, void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                             mla_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the current device's status
  * word.  Returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (or
  * MLA_ERR_CUDA if the synchronisation itself failed).  If detail is not NULL

@@ -15,6 +15,7 @@
 #include "decode_bf16.cuh"
 #include "gemm_bf16.cuh"
 #include "kernels_fp32.cuh"
+#include "prefill_bf16.cuh"
 #include "prologue.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
@@ -89,6 +90,9 @@ bool device_info(DeviceInfo& out) {
             return false;
         if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  200 * 1024) != cudaSuccess)
+            return false;
+        if (cudaFuncSetAttribute(mla::pre::prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mla::pre::SMEM_ALLOC) != cudaSuccess)
             return false;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (d.sms / 2), 1, 1);
@@ -236,14 +240,16 @@ size_t plain_gemm_ws_bytes(const GemmPlan& g) { return round256(g.ws_part_bytes)
 
 // out[n * ldo + m] = sum_k W[m, k] X[n, k] in bf16: the weight W [M, K]
 // (K-major) on the UMMA M axis, the activation rows X [N, K] on N.
+// X's rows are x_ld elements apart (0: K).
 mla_status_t plain_gemm(const void* W, const void* X, __nv_bfloat16* out, int64_t ldo, int M, int N,
-                        int K, const GemmPlan& g, void* ws, cudaStream_t st) {
+                        int K, const GemmPlan& g, void* ws, cudaStream_t st, int64_t x_ld = 0) {
     CUtensorMap ta, tx;
+    if (x_ld == 0) x_ld = K;
     cuuint64_t ad[3] = {(cuuint64_t)K, (cuuint64_t)M, 1};
     cuuint64_t as[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * M * 2};
     cuuint32_t ab[3] = {64, 128, 1};
     cuuint64_t xd[3] = {(cuuint64_t)K, 1, (cuuint64_t)N};
-    cuuint64_t xs[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * 2};
+    cuuint64_t xs[2] = {(cuuint64_t)x_ld * 2, (cuuint64_t)x_ld * 2};
     cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g.BN};
     if (!make_map(&ta, W, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tx, X, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
@@ -599,6 +605,110 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
     p.q_tmp = q_tmp;
     mla::pro::q_split_bf16_kernel<<<(unsigned)N, mla::pro::THREADS, sizeof(float) * (size_t)d_r, st>>>(p);
     return launch_status();
+}
+
+// ------------------------------------------------------------- prefill
+
+size_t mla_prefill_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t dtype) {
+    if (dtype != MLA_BF16 || rows < 1 || H < 1 || d_h < 1 || d < 128) return 0;
+    const int64_t K = (int64_t)H * d_h;
+    if (K > (1 << 30)) return 0;
+    DeviceInfo di;
+    if (!device_info(di)) return 0;
+    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, true));
+}
+
+mla_status_t mla_prefill_expand(const void* kv, const void* w_uk, const void* w_uv, void* k_nope,
+                                void* v, int rows, int H, int d_h, int d_c, int d_r,
+                                mla_dtype_t dtype, mla_stream_t stream) {
+    if (!kv || !w_uk || !w_uv || !k_nope || !v || rows < 1 || H < 1 || d_h < 1 || d_c < 1 || d_r < 0)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(kv) || !aligned16(w_uk) || !aligned16(w_uv) || !aligned16(k_nope) || !aligned16(v))
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16) return dtype == MLA_FP32 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    const int64_t M = (int64_t)H * d_h;
+    if (M % 128 != 0 || d_c % 64 != 0 || ((d_c + d_r) * 2) % 16 != 0 || M > (1 << 30))
+        return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // K_nope[r, i, :] = W^UK_i c_r and V[r, i, :] = W^UV_i c_r: the stacked
+    // [H * d_h x d_c] weight on the UMMA M axis, the latents c (the first d_c
+    // values of each cache row) on N, no split of the short reduction
+    const GemmPlan g = gemm_plan((int)M, rows, d_c, 1, di.sms, false);
+    mla_status_t s = plain_gemm(w_uk, kv, static_cast<__nv_bfloat16*>(k_nope), M, (int)M, rows, d_c, g,
+                                nullptr, st, d_c + d_r);
+    if (s != MLA_OK) return s;
+    return plain_gemm(w_uv, kv, static_cast<__nv_bfloat16*>(v), M, (int)M, rows, d_c, g, nullptr, st,
+                      d_c + d_r);
+}
+
+mla_status_t mla_prefill_attn(const void* q_nope, const void* q_pe, const void* k_nope,
+                              const void* kv, const void* v, int B, int L, int H, int d_h, int d_c,
+                              int d_r, float scale, int causal, void* u, float* lse,
+                              mla_dtype_t dtype, mla_stream_t stream) {
+    if (!q_nope || !q_pe || !k_nope || !kv || !v || !u || !lse) return MLA_ERR_INVALID_ARG;
+    if (B < 1 || L < 1 || H < 1 || d_h < 1 || d_c < 1 || d_r < 1 || !std::isfinite(scale))
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(k_nope) || !aligned16(kv) ||
+        !aligned16(v) || !aligned16(u))
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16) return dtype == MLA_FP32 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    if (d_h != mla::pre::DH || d_r != mla::pre::DR || d_c % 64 != 0) return MLA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)B * L;
+    if (rows > INT32_MAX - mla::pre::BK || H > 65535 || B > 65535) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    CUtensorMap tm_kn, tm_kr, tm_v;
+    {   // k_nope, v: [rows][H][128]; a box is 128 rows x 64 dims of one head
+        const cuuint64_t dims[3] = {(cuuint64_t)d_h, (cuuint64_t)H, (cuuint64_t)rows};
+        const cuuint64_t strides[2] = {(cuuint64_t)d_h * 2, (cuuint64_t)H * d_h * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)mla::pre::BK};
+        if (!make_map(&tm_kn, k_nope, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            !make_map(&tm_v, v, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return MLA_ERR_CUDA;
+    }
+    {   // the cache rows [c ; k^R]: the RoPE key is the 64 columns from d_c on
+        const cuuint64_t dims[2] = {(cuuint64_t)(d_c + d_r), (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)(d_c + d_r) * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)mla::pre::BK};
+        if (!make_map(&tm_kr, kv, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B)) return MLA_ERR_CUDA;
+    }
+    mla::pre::Params p;
+    p.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+    p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+    p.u = static_cast<__nv_bfloat16*>(u);
+    p.lse = lse;
+    p.B = B;
+    p.L = L;
+    p.H = H;
+    p.nqb = (L + mla::pre::BQ - 1) / mla::pre::BQ;
+    p.scale_log2 = scale * mla::dec::LOG2E;
+    p.causal = causal ? 1 : 0;
+    p.rope_col = d_c;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const dim3 grid((unsigned)p.nqb, (unsigned)H, (unsigned)B);
+    mla::pre::prefill_bf16_kernel<<<grid, mla::pre::THREADS, mla::pre::SMEM_ALLOC, st>>>(tm_kn, tm_kr,
+                                                                                         tm_v, p);
+    return launch_status();
+}
+
+mla_status_t mla_prefill_out(const void* u, const void* w_o, void* out, int rows, int H, int d_h,
+                             int d, void* workspace, size_t workspace_bytes, mla_dtype_t dtype,
+                             mla_stream_t stream) {
+    if (!u || !w_o || !out || rows < 1 || H < 1 || d_h < 1 || d < 1) return MLA_ERR_INVALID_ARG;
+    if (!aligned16(u) || !aligned16(w_o) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16) return dtype == MLA_FP32 ? MLA_ERR_UNSUPPORTED : MLA_ERR_INVALID_ARG;
+    const int64_t K = (int64_t)H * d_h;
+    if (d % 128 != 0 || K % 64 != 0 || K > (1 << 30)) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, true);
+    if (g.splits > 1 && (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g)))
+        return MLA_ERR_INVALID_ARG;
+    // out = W^O u: W^O [d x H * d_h] on the UMMA M axis, the rows of u on N
+    return plain_gemm(w_o, u, static_cast<__nv_bfloat16*>(out), d, d, rows, (int)K, g, workspace,
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------- mla_combine

@@ -28,7 +28,8 @@ SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_
            "mla_decode_plan", "mla_decode_attn_noalloc", "mla_decode_noalloc_max_bytes",
            "mla_cache_append_workspace_size", "mla_cache_append", "mla_project_q_workspace_size",
            "mla_project_q", "mla_fold_out_weights", "mla_out_proj_merged_workspace_size",
-           "mla_out_proj_merged", "mla_set_wait_limit", "mla_decode_attn_partial"]
+           "mla_out_proj_merged", "mla_set_wait_limit", "mla_decode_attn_partial",
+           "mla_prefill_expand", "mla_prefill_attn", "mla_prefill_workspace_size", "mla_prefill_out"]
 
 
 class MLAError(RuntimeError):
@@ -97,6 +98,14 @@ def _lib():
         lib.mla_out_proj_merged.restype = I
         lib.mla_decode_attn_partial.argtypes = lib.mla_decode_attn.argtypes
         lib.mla_decode_attn_partial.restype = I
+        lib.mla_prefill_expand.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
+        lib.mla_prefill_expand.restype = I
+        lib.mla_prefill_attn.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, P, P, I, P]
+        lib.mla_prefill_attn.restype = I
+        lib.mla_prefill_workspace_size.argtypes = [I, I, I, I, I]
+        lib.mla_prefill_workspace_size.restype = Z
+        lib.mla_prefill_out.argtypes = [P, P, P, I, I, I, I, P, Z, I, P]
+        lib.mla_prefill_out.restype = I
         lib.mla_set_wait_limit.argtypes = [ctypes.c_uint64]
         lib.mla_set_wait_limit.restype = I
         _LIB = lib
@@ -367,6 +376,57 @@ def get_device_status(stream=None) -> tuple[int, int]:
     detail = ctypes.c_uint32(0)
     code = _lib().mla_get_device_status(_stream(stream), ctypes.byref(detail))
     return int(code), int(detail.value)
+
+
+def prefill_expand(kv, w_uk, w_uv, k_nope=None, v=None, stream=None):
+    """Per-head keys and values of cache rows kv [rows, d_c+d_r]:
+    (k_nope, v) [rows, H, d_h] = (W^UK_i c, W^UV_i c)."""
+    rows, width = kv.shape
+    H, d_h, d_c = w_uk.shape
+    if k_nope is None:
+        k_nope = torch.empty((rows, H, d_h), dtype=kv.dtype, device=kv.device)
+    if v is None:
+        v = torch.empty((rows, H, d_h), dtype=kv.dtype, device=kv.device)
+    _check("mla_prefill_expand", _lib().mla_prefill_expand(
+        _ptr(kv), _ptr(w_uk), _ptr(w_uv), _ptr(k_nope), _ptr(v), rows, H, d_h, d_c, width - d_c,
+        _dt(kv), _stream(stream)))
+    return k_nope, v
+
+
+def prefill_attn(q_nope, q_pe, k_nope, kv, v, L: int, scale: float, causal: bool = True, u=None,
+                 lse=None, stream=None):
+    """Attention of B = rows / L sequences, every token a query; q_nope, k_nope,
+    v [rows, H, d_h], q_pe [rows, H, d_r], kv [rows, d_c+d_r].  Returns
+    (u [rows, H, d_h], lse [rows, H] fp32)."""
+    rows, H, d_h = q_nope.shape
+    d_r = q_pe.shape[2]
+    d_c = kv.shape[1] - d_r
+    if rows % L:
+        raise ValueError("rows must be a multiple of L")
+    if u is None:
+        u = torch.empty_like(q_nope)
+    if lse is None:
+        lse = torch.empty((rows, H), dtype=torch.float32, device=q_nope.device)
+    _check("mla_prefill_attn", _lib().mla_prefill_attn(
+        _ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(kv), _ptr(v), rows // L, L, H, d_h, d_c, d_r,
+        float(scale), int(bool(causal)), _ptr(u), _ptr(lse), _dt(q_nope), _stream(stream)))
+    return u, lse
+
+
+def prefill_out(u, w_o, out=None, workspace=None, stream=None):
+    """out [rows, d] = W^O u for u [rows, H, d_h], w_o [d, H*d_h]."""
+    rows, H, d_h = u.shape
+    d = w_o.shape[0]
+    if out is None:
+        out = torch.empty((rows, d), dtype=u.dtype, device=u.device)
+    need = int(_lib().mla_prefill_workspace_size(rows, H, d_h, d, _dt(u)))
+    if workspace is None and need > 0:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=u.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check("mla_prefill_out", _lib().mla_prefill_out(
+        _ptr(u), _ptr(w_o), _ptr(out), rows, H, d_h, d, _ptr(workspace), ws_bytes, _dt(u),
+        _stream(stream)))
+    return out
 
 
 def set_wait_limit(ns: int) -> None:

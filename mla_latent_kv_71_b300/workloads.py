@@ -17,6 +17,8 @@ stated, then rounded to the storage type with round-to-nearest-even):
 * Ragged lengths are drawn uniformly from [1, max_len] with the stated seed.
 * Projection weights are drawn N(0, 1/fan_in), fan_in being the input width
   of the map; hidden states are N(0, 1).
+* Prefill batches (every token a query): cache rows [c ; k^R], then q^C and
+  q^R, drawn N(0, 1) in that order, then W^UK, W^UV, W^O as above.
 """
 
 from __future__ import annotations
@@ -127,6 +129,33 @@ def q_nope(B: int, T: int, H: int, d_h: int, *, seed: int, device="cpu",
     g = _gen(seed, device)
     return torch.randn((B, T, H, d_h), generator=g, device=device,
                        dtype=torch.float32).to(dtype)
+
+
+@dataclass
+class PrefillCase:
+    """B sequences of L tokens, every token a query (tensors on ``device``)."""
+    kv: torch.Tensor       # [B*L, d_c + d_r] cache rows [c ; k^R]
+    q_nope: torch.Tensor   # [B*L, H, d_h]
+    q_pe: torch.Tensor     # [B*L, H, d_r]
+    w_uk: torch.Tensor     # [H, d_h, d_c]
+    w_uv: torch.Tensor     # [H, d_h, d_c]
+    w_o: torch.Tensor      # [d, H*d_h]
+    B: int
+    L: int
+    scale: float
+
+
+def prefill_case(B: int, L: int, H: int, *, d_h: int = 128, d_c: int = 512, d_r: int = 64,
+                 d: int = 7168, seed: int = 0, device="cpu", dtype=torch.bfloat16) -> PrefillCase:
+    g = _gen(seed, device)
+    kv = torch.randn((B * L, d_c + d_r), generator=g, device=device, dtype=torch.float32)
+    qn = torch.randn((B * L, H, d_h), generator=g, device=device, dtype=torch.float32)
+    qp = torch.randn((B * L, H, d_r), generator=g, device=device, dtype=torch.float32)
+    w_uk = weight((H, d_h, d_c), d_c, g, device, dtype)
+    w_uv = weight((H, d_h, d_c), d_c, g, device, dtype)
+    w_o = weight((d, H * d_h), H * d_h, g, device, dtype)
+    return PrefillCase(kv.to(dtype), qn.to(dtype), qp.to(dtype), w_uk, w_uv, w_o, B, L,
+                       1.0 / math.sqrt(d_h + d_r))
 
 
 def tiny_model(seed: int = 0, device="cpu"):
