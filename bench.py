@@ -544,6 +544,57 @@ def run_projections(args, local):
     return res
 
 
+def run_prefill(args, local):
+    """Training-form prefill (row f3) of one 4096-token sequence with the
+    DeepSeek-shaped attention (128 heads, d_h 128, d_c 512, d_r 64, d 7168),
+    each call timed alone like --projections (median of graph replays, L2
+    flushed before each).  The attention is bound by the tensor cores: its
+    work is the causal count of (query, key, head) triples x 640 FLOPs
+    (2 (d_h + d_r) for the score, 2 d_h for the weighted sum), against the
+    bf16 tensor peak.  The expansion (W^UK c, W^UV c) and W^O are GEMMs."""
+    from mla_latent_kv_71_b300 import mla
+    dev = torch.device("cuda", local)
+    B, L, H, d_h, d_c, d_r, d = 1, 4096, 128, 128, 512, 64, 7168
+    case = workloads.prefill_case(B, L, H, d=d, seed=111, device=dev)
+    rows = B * L
+    bf = torch.bfloat16
+    k = torch.empty((rows, H, d_h), dtype=bf, device=dev)
+    v = torch.empty_like(k)
+    u = torch.empty_like(k)
+    lse = torch.empty((rows, H), dtype=torch.float32, device=dev)
+    out = torch.empty((rows, d), dtype=bf, device=dev)
+    need = int(mla.library().mla_prefill_workspace_size(rows, H, d_h, d, mla.MLA_BF16))
+    ws = torch.zeros(max(1, need), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    pk, pk_kind = peaks()
+    triples = H * B * L * (L + 1) // 2
+    attn_flops = triples * (2 * (d_h + d_r) + 2 * d_h)
+    res = {"metric": "MLA training-form prefill attention TFLOP/s vs bf16 tensor peak",
+           "workload": f"prefill_b{B}_l{L}_h{H}", "B": B, "L": L, "H": H, "d_h": d_h, "d_c": d_c,
+           "d_r": d_r, "d": d, "causal": True, "dtype": "bf16", "data": "synthetic",
+           "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
+           "peak_bf16_tflops": pk["bf16_tflops"], "peak_kind": pk_kind}
+    us = time_alone(lambda: mla.prefill_expand(case.kv, case.w_uk, case.w_uv, k, v, stream=s), s, flush,
+                    args.steps, args.warmup)
+    fl = 2 * 2 * rows * H * d_h * d_c
+    res["expand"] = {"us": us, "flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
+                     "frac_tensor": fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"]}
+    us = time_alone(lambda: mla.prefill_attn(case.q_nope, case.q_pe, k, case.kv, v, L, case.scale, True,
+                                             u, lse, stream=s), s, flush, args.steps, args.warmup)
+    tf = attn_flops / (us * 1e-6) / 1e12
+    res["attention"] = {"us": us, "flops": attn_flops, "tflops": tf, "frac_tensor": tf / pk["bf16_tflops"]}
+    us = time_alone(lambda: mla.prefill_out(u, case.w_o, out, ws, stream=s), s, flush, args.steps,
+                    args.warmup)
+    fl = 2 * rows * d * H * d_h
+    res["out"] = {"us": us, "flops": fl, "tflops": fl / (us * 1e-6) / 1e12,
+                  "frac_tensor": fl / (us * 1e-6) / 1e12 / pk["bf16_tflops"]}
+    code, detail = mla.get_device_status()
+    if code != 0:
+        raise RuntimeError(f"device status {code} detail {detail:#x}")
+    return res
+
+
 def run_prologue(args, local):
     """The steps before the decode, each timed alone like --projections: the
     cache write of one new token per sequence of the headline batch (64
@@ -667,6 +718,8 @@ def main():
                     help="time mla_cache_append and mla_project_q alone (the cache write before the path)")
     ap.add_argument("--merged", action="store_true",
                     help="time mla_out_proj against mla_out_proj_merged (W^O W^UV merged ahead of time)")
+    ap.add_argument("--prefill", action="store_true",
+                    help="time the training-form prefill (expansion, causal attention, W^O) of 4096 tokens")
     ap.add_argument("--ref-step-s", type=float, default=5.0,
                     help="reference arm: CPU seconds per step (sample size)")
     args = ap.parse_args()
@@ -684,6 +737,10 @@ def main():
     if args.merged:
         if rank == 0:
             print(json.dumps(run_merged(args, local)), flush=True)
+        return
+    if args.prefill:
+        if rank == 0:
+            print(json.dumps(run_prefill(args, local)), flush=True)
         return
     if args.impl == "reference":
         if rank == 0:

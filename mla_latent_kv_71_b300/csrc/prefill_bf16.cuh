@@ -20,8 +20,11 @@
 // TMEM (512 columns): S double-buffered at [0,128) and [128,256), O at
 // [256,384), Q at [384,480).  Block j's P (bf16 pairs) overwrites the first
 // 64 columns of its own S buffer once the softmax has its scores in
-// registers.  Keys and values stream through a 2-stage TMA ring; the query
-// rows are loaded by the softmax threads (one row each) into TMEM.
+// registers.  Keys and values stream through separate TMA rings: a key
+// block is released once its score product is done (three stages, so keys
+// run well ahead), a value block once its P . V product is (two stages);
+// the query rows are loaded by the softmax threads (one row each) into
+// TMEM.
 //
 // Warp roles (192 threads):
 //   warp 0      TMA producer: K (content part per head, RoPE part shared)
@@ -49,16 +52,17 @@ constexpr int BQ = 128;        // queries per CTA (UMMA M)
 constexpr int BK = 128;        // keys per block (UMMA N of S, K of O)
 constexpr int DH = 128;        // content dims of q and k; dims of v
 constexpr int DR = 64;         // RoPE dims
-constexpr int NSTAGE = 2;
+constexpr int NK = 3;           // key stages
+constexpr int NV = 2;           // value stages
 constexpr int THREADS = 192;
 constexpr int SM_WARP0 = 2;    // softmax warps 2..5
 
 constexpr uint32_t BOX_BYTES = BK * 128;                 // 128 rows x 64 bf16 (128-byte swizzle)
 constexpr uint32_t K_BYTES = 3 * BOX_BYTES;              // content 0..63, 64..127, RoPE 0..63
 constexpr uint32_t V_BYTES = 2 * BOX_BYTES;              // dims 0..63, 64..127
-constexpr uint32_t STAGE_BYTES = K_BYTES + V_BYTES;      // 80 KB
-constexpr uint32_t OFF_BAR = NSTAGE * STAGE_BYTES;
-constexpr uint32_t NUM_BARS = 2 * NSTAGE + 2 + 2 + 1 + 1 + 1;
+constexpr uint32_t OFF_V = NK * K_BYTES;                 // 144 KB of keys, then 64 KB of values
+constexpr uint32_t OFF_BAR = OFF_V + NV * V_BYTES;
+constexpr uint32_t NUM_BARS = 2 * NK + 2 * NV + 2 + 2 + 1 + 1 + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr uint32_t SMEM_ALLOC = OFF_MISC + 64 + 1024;
 
@@ -104,20 +108,27 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_kn,   // k_nope [B*L]
 
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    auto FULL = [&](int s) { return BAR(s); };              // K and V of a block landed (TMA)
-    auto EMPTY = [&](int s) { return BAR(NSTAGE + s); };    // O(j) done reading V(j), S(j) done with K(j)
-    auto S_FULL = [&](int b) { return BAR(2 * NSTAGE + b); };  // S(j) in buffer j % 2 (commit)
-    auto P_FULL = [&](int b) { return BAR(2 * NSTAGE + 2 + b); };  // P(j) in TMEM (4 warps)
-    const uint32_t O_DONE = BAR(2 * NSTAGE + 4);            // O += P(j) V(j) done (commit, phase j)
-    const uint32_t Q_FULL = BAR(2 * NSTAGE + 5);            // query rows in TMEM (4 warps)
-    const uint32_t DRAIN = BAR(2 * NSTAGE + 6);             // teardown: every product finished
+    auto K_FULL = [&](int s) { return BAR(s); };            // K(j) landed (TMA), stage j % NK
+    auto K_EMPTY = [&](int s) { return BAR(NK + s); };      // S(j) done reading K(j) (commit)
+    auto V_FULL = [&](int s) { return BAR(2 * NK + s); };   // V(j) landed (TMA), stage j % NV
+    auto V_EMPTY = [&](int s) { return BAR(2 * NK + NV + s); };  // O(j) done reading V(j) (commit)
+    constexpr int NB0 = 2 * NK + 2 * NV;
+    auto S_FULL = [&](int b) { return BAR(NB0 + b); };      // S(j) in buffer j % 2 (commit)
+    auto P_FULL = [&](int b) { return BAR(NB0 + 2 + b); };  // P(j) in TMEM (4 warps)
+    const uint32_t O_DONE = BAR(NB0 + 4);                   // O += P(j) V(j) done (commit, phase j)
+    const uint32_t Q_FULL = BAR(NB0 + 5);                   // query rows in TMEM (4 warps)
+    const uint32_t DRAIN = BAR(NB0 + 6);                    // teardown: every product finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int* flag = reinterpret_cast<int*>(smem + OFF_MISC + 8);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(FULL(s), 1);
-            mbar_init(EMPTY(s), 1);
+        for (int s = 0; s < NK; ++s) {
+            mbar_init(K_FULL(s), 1);
+            mbar_init(K_EMPTY(s), 1);
+        }
+        for (int s = 0; s < NV; ++s) {
+            mbar_init(V_FULL(s), 1);
+            mbar_init(V_EMPTY(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(S_FULL(b), 1);
@@ -143,26 +154,36 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_kn,   // k_nope [B*L]
 
     if (warp == 0) {
         // ========================================================= producer
-        int it = 0;
+        // K(j) then V(j) for each block in turn: a key stage is free once
+        // the score product three blocks back is done, a value stage once
+        // the P . V product two back is.
+        int nk = 0, nv = 0;  // copies issued
         bool ok = !skip;
         if (lane == 0 && ok) {
-            for (int j = 0; j < nkb; ++j, ++it) {
-                const int s = j % NSTAGE;
-                if (!mbar_wait(EMPTY(s), (uint32_t)((j / NSTAGE) & 1) ^ 1u, 0x601)) { ok = false; break; }
-                const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+            for (int j = 0; j < nkb; ++j) {
                 const int y = (int)(tok0 + (int64_t)j * BK);  // first key row of the block
-                mbar_arrive_expect_tx(FULL(s), STAGE_BYTES);
+                const int sk = j % NK, sv = j % NV;
+                if (!mbar_wait(K_EMPTY(sk), (uint32_t)((j / NK) & 1) ^ 1u, 0x601)) { ok = false; break; }
+                const uint32_t kst = smem_u32(smem + sk * K_BYTES);
+                mbar_arrive_expect_tx(K_FULL(sk), K_BYTES);
                 // keys and values are read again by the head's other query
                 // blocks: loaded with the normal L2 policy
-                tma_load_3d_plain(st, &tm_kn, FULL(s), 0, head, y);
-                tma_load_3d_plain(st + BOX_BYTES, &tm_kn, FULL(s), 64, head, y);
-                tma_load_2d_plain(st + 2 * BOX_BYTES, &tm_kr, FULL(s), p.rope_col, y);
-                tma_load_3d_plain(st + K_BYTES, &tm_v, FULL(s), 0, head, y);
-                tma_load_3d_plain(st + K_BYTES + BOX_BYTES, &tm_v, FULL(s), 64, head, y);
+                tma_load_3d_plain(kst, &tm_kn, K_FULL(sk), 0, head, y);
+                tma_load_3d_plain(kst + BOX_BYTES, &tm_kn, K_FULL(sk), 64, head, y);
+                tma_load_2d_plain(kst + 2 * BOX_BYTES, &tm_kr, K_FULL(sk), p.rope_col, y);
+                ++nk;
+                if (!mbar_wait(V_EMPTY(sv), (uint32_t)((j / NV) & 1) ^ 1u, 0x602)) { ok = false; break; }
+                const uint32_t vst = smem_u32(smem + OFF_V + sv * V_BYTES);
+                mbar_arrive_expect_tx(V_FULL(sv), V_BYTES);
+                tma_load_3d_plain(vst, &tm_v, V_FULL(sv), 0, head, y);
+                tma_load_3d_plain(vst + BOX_BYTES, &tm_v, V_FULL(sv), 64, head, y);
+                ++nv;
             }
             // every copy issued here lands before the CTA can exit
-            for (int i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
-                mbar_wait_teardown(FULL(i % NSTAGE), (uint32_t)((i / NSTAGE) & 1), MLA_WAIT_LIMIT_NS);
+            for (int i = (nk > NK ? nk - NK : 0); i < nk; ++i)
+                mbar_wait_teardown(K_FULL(i % NK), (uint32_t)((i / NK) & 1), MLA_WAIT_LIMIT_NS);
+            for (int i = (nv > NV ? nv - NV : 0); i < nv; ++i)
+                mbar_wait_teardown(V_FULL(i % NV), (uint32_t)((i / NV) & 1), MLA_WAIT_LIMIT_NS);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -170,21 +191,22 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_kn,   // k_nope [B*L]
         bool ok = !skip;
         bool issued = false;
         const uint64_t dk0 = smem_desc(smem_u32(smem), 16, 1024, SWZ_128B);
-        const uint64_t dv0 = smem_desc(smem_u32(smem + K_BYTES), BOX_BYTES, 1024, SWZ_128B);
+        const uint64_t dv0 = smem_desc(smem_u32(smem + OFF_V), BOX_BYTES, 1024, SWZ_128B);
         auto issue_s = [&](int j) -> bool {  // S(j) = Q . K(j)^T into buffer j % 2
-            const int s = j % NSTAGE;
-            if (!__all_sync(0xffffffffu, mbar_wait(FULL(s), (uint32_t)((j / NSTAGE) & 1), 0x611))) return false;
+            const int s = j % NK;
+            if (!__all_sync(0xffffffffu, mbar_wait(K_FULL(s), (uint32_t)((j / NK) & 1), 0x611))) return false;
             // buffer j % 2 last held P(j - 2), which O(j - 2) has read
             if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(O_DONE, (uint32_t)((j - 2) & 1), 0x612)))
                 return false;
             tc_fence_after();
             if (elect_one_sync()) {
-                const uint64_t dk = dk0 + ((uint64_t)(s * STAGE_BYTES) >> 4);
+                const uint64_t dk = dk0 + ((uint64_t)(s * K_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < 12; ++k)  // 192 features: 3 boxes x 4 steps of 16
                     mma_ts(tmem + TM_S + BK * (j & 1), tmem + TM_Q + 8 * k,
                            dk + (uint64_t)(((k / 4) * BOX_BYTES + (k % 4) * 32) >> 4), IDESC_QK, k > 0 ? 1u : 0u);
                 tc_commit(S_FULL(j & 1));
+                tc_commit(K_EMPTY(s));
             }
             __syncwarp();
             issued = true;
@@ -196,15 +218,16 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_kn,   // k_nope [B*L]
             if (j + 1 < nkb && !(ok = issue_s(j + 1))) break;
             // O += P(j) . V(j) once P(j) is in TMEM (and O rescaled, if it was)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(P_FULL(j & 1), (uint32_t)((j >> 1) & 1), 0x613)))) break;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(V_FULL(j % NV), (uint32_t)((j / NV) & 1), 0x614)))) break;
             tc_fence_after();
             if (elect_one_sync()) {
-                const uint64_t dv = dv0 + ((uint64_t)((j % NSTAGE) * STAGE_BYTES) >> 4);
+                const uint64_t dv = dv0 + ((uint64_t)((j % NV) * V_BYTES) >> 4);
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k)  // 16 keys per step: 8 P columns, 2 KB of V
                     mma_ts(tmem + TM_O, tmem + TM_S + BK * (j & 1) + 8 * k, dv + (uint64_t)((k * 2048) >> 4),
                            IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
                 tc_commit(O_DONE);
-                tc_commit(EMPTY(j % NSTAGE));
+                tc_commit(V_EMPTY(j % NV));
             }
             __syncwarp();
         }
