@@ -663,7 +663,9 @@ def run_merged(args, local):
     rows, 128 heads, d_h 128, d_c 512, d 7168), each timed like
     --projections: W^UV and W^O kept apart (mla_out_proj, 252 MB of
     weights) and merged ahead of time (mla_out_proj_merged, one 7168 x 65536
-    matrix, 940 MB) -- the trade the pages weigh."""
+    matrix, 940 MB) -- the trade the pages weigh; and the query side the same
+    way (W^UQ and W^UK apart, 92 MB with W^Q's RoPE rows, against the folded
+    W^UK^T W^UQ, 201 MB)."""
     from mla_latent_kv_71_b300 import mla
     dev = torch.device("cuda", local)
     spec = workloads.WORKLOADS["mtp_b32_t2_l8192"]
@@ -698,6 +700,38 @@ def run_merged(args, local):
         res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
                      "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12}
     res["merged_over_apart_time"] = res["out_proj_merged"]["us"] / res["out_proj"]["us"]
+    # The query side: c^Q (1536 wide) -> q_lat, W^UQ then W^UK apart
+    # (mla_project_q's content and RoPE rows, then mla_absorb_q) against the
+    # folded W^UK^T W^UQ (mla_absorb_q_merged; the RoPE rows of W^Q are
+    # still needed for q^R and are timed on their own here, as a project_q of
+    # a W^Q with only those rows per head would cost).
+    d_q, d_r = 1536, 64
+    gq = torch.Generator(device=dev).manual_seed(spec["seed"] + 6000)
+    w_q = workloads.weight((H * (d_h + d_r), d_q), d_q, gq, dev, bf)
+    w_uk = workloads.weight((H, d_h, d_c), d_c, gq, dev, bf)
+    c_q = torch.randn((rows, d_q), generator=gq, device=dev).to(bf)
+    pos = torch.full((rows,), 4096, dtype=torch.int32, device=dev)
+    wq_m = mla.fold_q_weights(w_uk, w_q, d_r)
+    q_nope = torch.empty((rows, H, d_h), dtype=bf, device=dev)
+    q_pe = torch.empty((rows, H, d_r), dtype=bf, device=dev)
+    q_lat = torch.empty((rows, H, d_c), dtype=bf, device=dev)
+    ws_q = torch.zeros(max(1, mla.project_q_workspace_size(rows, H, d_h, d_r, d_q)), dtype=torch.uint8,
+                       device=dev)
+    t_pq = time_alone(lambda: mla.project_q(c_q, w_q, pos, H, d_h, d_r, q_nope, q_pe, workspace=ws_q,
+                                            stream=s), s, flush, args.steps, args.warmup)
+    t_ab = time_alone(lambda: mla.absorb_q(q_nope, w_uk, q_lat.view(rows, H, d_c), stream=s), s, flush,
+                      args.steps, args.warmup)
+    t_m = time_alone(lambda: mla.absorb_q_merged(c_q, wq_m, q_lat, stream=s), s, flush, args.steps,
+                     args.warmup)
+    apart_w = (w_q.numel() + w_uk.numel()) * 2
+    merged_w = wq_m.numel() * 2
+    res["query_apart"] = {"us": t_pq + t_ab, "project_q_us": t_pq, "absorb_q_us": t_ab,
+                          "weight_bytes": apart_w, "gbs": apart_w / ((t_pq + t_ab) * 1e-6) / 1e9}
+    res["query_merged_content"] = {"us": t_m, "weight_bytes": merged_w,
+                                   "gbs": merged_w / (t_m * 1e-6) / 1e9,
+                                   "frac_hbm": merged_w / (t_m * 1e-6) / 1e9 / pk["hbm_gbs"],
+                                   "note": "content part only; q^R still needs the RoPE rows of W^Q"}
+    res["query_merged_over_apart_time"] = t_m / (t_pq + t_ab)
     code, detail = mla.get_device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} detail {detail:#x}")

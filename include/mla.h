@@ -347,6 +347,37 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
                            mla_stream_t stream);
 
 /*
+ * Query-side weight merge ([Mishra] "Multi-head Latent Attention": the
+ * up-projections fold once, offline, W^UK_i^T W^UQ_i; [Zhang] "Matrix
+ * absorption: compression that also saves compute").  With the compressed
+ * query c^Q (d_q wide) and W^UQ_i the content rows of head i's block of W^Q,
+ *     q_lat_i = W^UK_i^T (W^UQ_i c^Q) = (W^UK_i^T W^UQ_i) c^Q
+ * so the two products of the unmerged path (mla_project_q's content part,
+ * then mla_absorb_q) become one, against a weight of H * d_c * d_q values in
+ * place of H * d_h * (d_q + d_c).  The RoPE part of the query still comes
+ * from W^QR (mla_project_q).
+ *
+ * mla_fold_q_weights -- w_merged [d_q, H, d_c]: w_merged[k, i, c] =
+ *   sum_e W^UK_i[e, c] W^UQ_i[e, k].
+ *   w_uk  [H, d_h, d_c];  w_q [H * (d_h + d_r), d_q] (head i: d_h content
+ *   rows, then d_r RoPE rows, as for mla_project_q)
+ *   workspace >= mla_fold_q_workspace_size(H, d_h, d_q, dtype) bytes
+ * bf16 as mla_absorb_q (d_c % 128 == 0, d_h % 64 == 0); fp32 any size.
+ */
+size_t mla_fold_q_workspace_size(int H, int d_h, int d_q, mla_dtype_t dtype);
+mla_status_t mla_fold_q_weights(const void* w_uk, const void* w_q, void* w_merged, int H, int d_h,
+                                int d_r, int d_c, int d_q, void* workspace, size_t workspace_bytes,
+                                mla_dtype_t dtype, mla_stream_t stream);
+
+/*
+ * mla_absorb_q_merged -- q_lat [rows, H, d_c] = W_merged c^Q for c^Q
+ * [rows, d_q] and w_merged [d_q, H, d_c] from mla_fold_q_weights.
+ * bf16: H * d_c % 128 == 0, d_q % 64 == 0 (tensor cores); fp32 any size.
+ */
+mla_status_t mla_absorb_q_merged(const void* c_q, const void* w_merged, void* q_lat, int rows, int H,
+                                 int d_c, int d_q, mla_dtype_t dtype, mla_stream_t stream);
+
+/*
  * Prefill in the training (unabsorbed) form ([Mishra] "Multi-head Latent
  * Attention": the unabsorbed form is the one used in training; [llms]
  * "Low-Rank Key-Value Joint Compression" for the up-projections and "The

@@ -13,6 +13,7 @@
 
 #include "../../include/mla.h"
 #include "decode_bf16.cuh"
+#include "fold_q.cuh"
 #include "gemm_bf16.cuh"
 #include "kernels_fp32.cuh"
 #include "prefill_bf16.cuh"
@@ -429,6 +430,73 @@ mla_status_t mla_fold_out_weights(const void* w_uv, const void* w_o, void* w_mer
     // W_merged[n, i, :] = W^UV_i^T W^O[n, i, :] is the query absorption's
     // product with row n of W^O, head slice i, in the place of q^C.
     return mla_absorb_q(w_o, w_uv, w_merged, d, H, d_h, d_c, dtype, stream);
+}
+
+size_t mla_fold_q_workspace_size(int H, int d_h, int d_q, mla_dtype_t dtype) {
+    if ((dtype != MLA_BF16 && dtype != MLA_FP32) || H < 1 || d_h < 1 || d_q < 1) return 0;
+    return round256((size_t)d_q * H * d_h * (dtype == MLA_BF16 ? 2 : 4));
+}
+
+mla_status_t mla_fold_q_weights(const void* w_uk, const void* w_q, void* w_merged, int H, int d_h,
+                                int d_r, int d_c, int d_q, void* workspace, size_t workspace_bytes,
+                                mla_dtype_t dtype, mla_stream_t stream) {
+    if (!w_uk || !w_q || !w_merged || H < 1 || d_h < 1 || d_r < 0 || d_c < 1 || d_q < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
+    if (!workspace || !aligned16(workspace) ||
+        workspace_bytes < mla_fold_q_workspace_size(H, d_h, d_q, dtype))
+        return MLA_ERR_INVALID_ARG;
+    if ((int64_t)H * d_h > 65535 * 32 || d_q > 65535 * 32) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // W^UQ^T [d_q, H, d_h] into the workspace, then the query absorption of
+    // its d_q rows: row k, head slice i becomes W^UK_i^T W^UQ_i[:, k]
+    const dim3 grid((unsigned)((d_q + 31) / 32), (unsigned)((H * d_h + 31) / 32));
+    const dim3 block(32, 8);
+    if (dtype == MLA_BF16)
+        mla::foldq::uq_transpose_kernel<__nv_bfloat16><<<grid, block, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(w_q), static_cast<__nv_bfloat16*>(workspace), H, d_h, d_r,
+            d_q);
+    else
+        mla::foldq::uq_transpose_kernel<float><<<grid, block, 0, st>>>(
+            static_cast<const float*>(w_q), static_cast<float*>(workspace), H, d_h, d_r, d_q);
+    if (launch_status() != MLA_OK) return MLA_ERR_CUDA;
+    return mla_absorb_q(workspace, w_uk, w_merged, d_q, H, d_h, d_c, dtype, stream);
+}
+
+mla_status_t mla_absorb_q_merged(const void* c_q, const void* w_merged, void* q_lat, int rows, int H,
+                                 int d_c, int d_q, mla_dtype_t dtype, mla_stream_t stream) {
+    if (!c_q || !w_merged || !q_lat || rows < 1 || H < 1 || d_c < 1 || d_q < 1)
+        return MLA_ERR_INVALID_ARG;
+    if (!aligned16(c_q) || !aligned16(w_merged) || !aligned16(q_lat)) return MLA_ERR_INVALID_ARG;
+    const int64_t M = (int64_t)H * d_c;
+    if (M > (1 << 30) || rows > 65535) return MLA_ERR_UNSUPPORTED;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dtype == MLA_FP32) {
+        const dim3 grid((unsigned)((M + 127) / 128), (unsigned)rows);
+        mla::foldq::q_merged_fp32_kernel<<<grid, 128, 0, st>>>(
+            static_cast<const float*>(c_q), static_cast<const float*>(w_merged), static_cast<float*>(q_lat),
+            (int)M, d_q);
+        return launch_status();
+    }
+    if (dtype != MLA_BF16) return MLA_ERR_INVALID_ARG;
+    if (M % 128 != 0 || d_q % 64 != 0) return MLA_ERR_UNSUPPORTED;
+    DeviceInfo di;
+    if (!device_info(di)) return MLA_ERR_CUDA;
+    // q_lat = W_merged c^Q: the folded weight [d_q, H * d_c] is stored along
+    // its output axis, so it is an MN-major A operand of the GEMM
+    const GemmPlan g = gemm_plan((int)M, rows, d_q, 1, di.sms, false);
+    CUtensorMap ta, tx;
+    cuuint64_t ad[3] = {(cuuint64_t)M, (cuuint64_t)d_q, 1};
+    cuuint64_t as[2] = {(cuuint64_t)M * 2, (cuuint64_t)M * d_q * 2};
+    cuuint32_t ab[3] = {64, 64, 1};
+    cuuint64_t xd[3] = {(cuuint64_t)d_q, 1, (cuuint64_t)rows};
+    cuuint64_t xs[2] = {(cuuint64_t)d_q * 2, (cuuint64_t)d_q * 2};
+    cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g.BN};
+    if (!make_map(&ta, w_merged, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tx, c_q, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
+        return MLA_ERR_CUDA;
+    return launch_gemm(ta, tx, (int)M, rows, d_q, 1, 1, 0, g, static_cast<__nv_bfloat16*>(q_lat), M, 0,
+                       nullptr, nullptr, st);
 }
 
 size_t mla_out_proj_merged_workspace_size(int rows, int H, int d_c, int d, mla_dtype_t dtype) {

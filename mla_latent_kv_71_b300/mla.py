@@ -29,7 +29,8 @@ SYMBOLS = ["mla_absorb_q", "mla_decode_workspace_size", "mla_decode_attn", "mla_
            "mla_cache_append_workspace_size", "mla_cache_append", "mla_project_q_workspace_size",
            "mla_project_q", "mla_fold_out_weights", "mla_out_proj_merged_workspace_size",
            "mla_out_proj_merged", "mla_set_wait_limit", "mla_decode_attn_partial",
-           "mla_prefill_expand", "mla_prefill_attn", "mla_prefill_workspace_size", "mla_prefill_out"]
+           "mla_prefill_expand", "mla_prefill_attn", "mla_prefill_workspace_size", "mla_prefill_out",
+           "mla_fold_q_workspace_size", "mla_fold_q_weights", "mla_absorb_q_merged"]
 
 
 class MLAError(RuntimeError):
@@ -106,6 +107,12 @@ def _lib():
         lib.mla_prefill_workspace_size.restype = Z
         lib.mla_prefill_out.argtypes = [P, P, P, I, I, I, I, P, Z, I, P]
         lib.mla_prefill_out.restype = I
+        lib.mla_fold_q_workspace_size.argtypes = [I, I, I, I]
+        lib.mla_fold_q_workspace_size.restype = Z
+        lib.mla_fold_q_weights.argtypes = [P, P, P, I, I, I, I, I, P, Z, I, P]
+        lib.mla_fold_q_weights.restype = I
+        lib.mla_absorb_q_merged.argtypes = [P, P, P, I, I, I, I, I, P]
+        lib.mla_absorb_q_merged.restype = I
         lib.mla_set_wait_limit.argtypes = [ctypes.c_uint64]
         lib.mla_set_wait_limit.restype = I
         _LIB = lib
@@ -376,6 +383,33 @@ def get_device_status(stream=None) -> tuple[int, int]:
     detail = ctypes.c_uint32(0)
     code = _lib().mla_get_device_status(_stream(stream), ctypes.byref(detail))
     return int(code), int(detail.value)
+
+
+def fold_q_weights(w_uk, w_q, d_r: int, w_merged=None, workspace=None, stream=None):
+    """W_merged [d_q, H, d_c] with [k, i, :] = W^UK_i^T W^UQ_i[:, k]; w_uk
+    [H, d_h, d_c], w_q [H*(d_h+d_r), d_q]."""
+    H, d_h, d_c = w_uk.shape
+    d_q = w_q.shape[1]
+    if w_merged is None:
+        w_merged = torch.empty((d_q, H, d_c), dtype=w_uk.dtype, device=w_uk.device)
+    need = int(_lib().mla_fold_q_workspace_size(H, d_h, d_q, _dt(w_uk)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=w_uk.device)
+    _check("mla_fold_q_weights", _lib().mla_fold_q_weights(
+        _ptr(w_uk), _ptr(w_q), _ptr(w_merged), H, d_h, d_r, d_c, d_q, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _dt(w_uk), _stream(stream)))
+    return w_merged
+
+
+def absorb_q_merged(c_q, w_merged, q_lat=None, stream=None):
+    """q_lat [rows, H, d_c] = W_merged c^Q; c_q [rows, d_q], w_merged [d_q, H, d_c]."""
+    rows, d_q = c_q.shape
+    _, H, d_c = w_merged.shape
+    if q_lat is None:
+        q_lat = torch.empty((rows, H, d_c), dtype=c_q.dtype, device=c_q.device)
+    _check("mla_absorb_q_merged", _lib().mla_absorb_q_merged(
+        _ptr(c_q), _ptr(w_merged), _ptr(q_lat), rows, H, d_c, d_q, _dt(c_q), _stream(stream)))
+    return q_lat
 
 
 def prefill_expand(kv, w_uk, w_uv, k_nope=None, v=None, stream=None):
