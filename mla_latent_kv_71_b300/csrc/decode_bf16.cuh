@@ -591,7 +591,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
 
     if (warp == 0) {
         // ========================================================= producer
-        const uint64_t pol = l2_policy_evict_first();
+        // A page read once can leave L2 first; a page every query token (and
+        // head group) of its sequence reads -- the next unit, a cluster or
+        // two away on the line, reads it some 20 pages later -- stays.
+        const uint64_t pol = p.T * p.HG > 1 ? l2_policy_evict_last() : l2_policy_evict_first();
         int64_t it = 0;
         uint32_t tail_phase = 0;
         bool ok = !skip;

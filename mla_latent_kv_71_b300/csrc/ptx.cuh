@@ -139,6 +139,12 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return p;
 }
 
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // Bring `bytes` (a multiple of 16) of global memory at a 16-byte aligned
 // address into L2, asynchronously.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
