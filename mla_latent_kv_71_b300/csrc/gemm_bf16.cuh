@@ -1,23 +1,33 @@
-// gemm_bf16.cuh -- weight-streaming tcgen05 GEMM for the projections around
-// the absorbed decode: W^UK^T q (mla_absorb_q), W^UV o and W^O v
-// (mla_out_proj).
+// gemm_bf16.cuh -- persistent weight-streaming tcgen05 GEMM for the
+// projections around the attention: W^UK^T q (mla_absorb_q), W^UV o and W^O v
+// (mla_out_proj), the prologue's W^DKV h, W^KR h and W^Q h, the prefill
+// expansion and output, and the merged-weight variants.
+//
+//     D_z[m, n] = sum_k A_z[m, k] * X_z[n, k]        (z = head, or 0)
 //
 // In decode the activations are a few dozen rows (B*T) while the weights are
-// megabytes, so the weight's output dimension is placed on the UMMA M axis
-// (128 lanes of TMEM) and the activation rows on N ("swap AB"):
+// megabytes, so the weight's output dimension sits on the UMMA M axis (128
+// TMEM lanes) and the activation rows on N ("swap AB").  A is read by TMA in
+// 128 x 64 tiles, K-major or MN-major (W^UK, whose stored rows run along
+// d_c); X is K-major, BN rows x 64 per stage.
 //
-//     D[m, n] = sum_k A_z[m, k] * X_z[n, k]        (z = head, or 0)
+// Work is cut into items (head z, N tile, K split, M tile), M tile fastest.
+// One CTA per SM walks a contiguous range of items with one continuous TMA
+// ring, so the copies of the next item start while the current one is still
+// being multiplied, and the accumulator is double-buffered in TMEM so the
+// epilogue of item i runs while the products of item i+1 are issued.
 //
-// A (weight) is read once from HBM by TMA in 128 x 64 tiles, either K-major
-// (rows of A contiguous along k) or MN-major (contiguous along m, as for
-// W^UK whose stored rows run along d_c); X is K-major.  The accumulator
-// tile [128 x BN] lives in TMEM.  A split-K grid dimension spreads long
-// reductions (W^O: K = H*d_h) over more SMs; the last CTA of a tile to finish
-// adds the fp32 partials in a fixed order and writes the bf16 result.
+// Roles (192 threads): warp 0 (one lane) issues TMA; warp 1 owns TMEM and
+// issues UMMA from an elected lane; warps 2..5 run the epilogue, warp w
+// reading TMEM lanes 32 (w % 4) .. +31.  The epilogue stages 32 accumulator
+// columns at a time through shared memory, so that every global store is a
+// 16-byte piece of a contiguous output row.
 //
-// Roles: warp 0 lane 0 issues TMA, warp 1 lane 0 issues UMMA (warp 1 also
-// owns the TMEM allocation), then all four warps run the epilogue (warp w
-// reads TMEM lanes 32w..32w+31).
+// Output modes: OUT_BF16 (no split: bf16 rows of D), OUT_REDUCE (split-K:
+// each split's fp32 partial goes to the workspace, and the last CTA to finish
+// a tile adds the splits in split order and writes bf16), OUT_PARTS (every
+// split's fp32 partial to the workspace, added up by the caller's next
+// kernel, which also applies its own epilogue).
 #pragma once
 
 #include <cstdint>
@@ -32,201 +42,367 @@ namespace gemm {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int STAGES = 4;  // pipeline depth (fewer when a CTA has fewer K chunks)
-constexpr int THREADS = 128;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB per stage
+constexpr int MAX_STAGES = 8;
+constexpr int THREADS = 192;
+constexpr int EPI_WARP0 = 2;
+constexpr int A_BYTES = BM * BK * 2;            // 16 KB per stage
+constexpr int EPI_COLS = 32;                    // accumulator columns staged per round
+constexpr int STG_BYTES = EPI_COLS * BM * 4;    // 16 KB (fp32 rows of 128)
+constexpr uint32_t SMEM_CAP = 227 * 1024;
+
+enum : int { OUT_BF16 = 0, OUT_REDUCE = 1, OUT_PARTS = 2 };
 
 struct Params {
-    int M, N, K;          // D is M x N, reduction length K (multiples of BM / BK)
-    int BN;               // N tile (multiple of 16, <= 256)
-    int n_tiles;          // ceil(N / BN)
+    int M;                // rows of D that exist (a multiple of 8; the last M tile may be partial)
+    int N, K;             // columns of D; reduction length (a multiple of BK)
+    int m_tiles;          // ceil(M / BM)
+    int m_split;          // M tiles >= m_split load A from the second map, at row (mt - m_split) * BM
+    int BN, n_tiles;      // N tile (multiple of 16, <= 256) and ceil(N / BN)
     int a_mn;             // A stored MN-major
     int x_batched;        // X has a head coordinate (z); else z = 0 for X
-    int splits;           // split-K factor (grid.z)
-    int chunks_per_split; // K chunks (of BK) per split
-    int stages;           // pipeline stages in shared memory, 1..STAGES
-    __nv_bfloat16* out;   // out[(n0+n) * ldo + z * out_z + m0 + m]
+    int splits;           // K splits
+    int chunks_per_split; // K chunks (of BK) per split; the last split may be shorter
+    int items;            // Z * n_tiles * splits * m_tiles
+    int stages;           // TMA ring depth, 1..MAX_STAGES
+    int mode;             // OUT_BF16 / OUT_REDUCE / OUT_PARTS
+    int a_evict_first;    // A is read once (one N tile): let it leave L2 first
+    int vec_out;          // out, ldo and out_z allow 16-byte stores
+    __nv_bfloat16* out;   // out[(n0+n) * ldo + z * out_z + m]
     int64_t ldo, out_z;
-    float* ws_part;       // [splits][Z][N][M] fp32 partials (split-K only)
-    int* ws_count;        // [Z * n_tiles * (M / BM)] arrival counters (split-K only)
+    float* ws_part;       // [splits][Z][N][M] fp32 partials (OUT_REDUCE, OUT_PARTS)
+    int* ws_count;        // [Z * n_tiles * m_tiles] arrival counters (OUT_REDUCE), zero between calls
 };
 
-__device__ __forceinline__ uint32_t x_bytes(int BN) { return (uint32_t)BN * BK * 2; }
+struct Item {
+    int z, nt, split, mt, kc0, kc1;
+};
 
-// At most 128 registers, so that up to four CTAs fit an SM when the
-// pipeline is short (a short K leaves each CTA little to load: more CTAs in
-// flight hide the TMA round trip).
-__global__ void __launch_bounds__(THREADS, 4)
-wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_x,
-             const Params p) {
+__device__ __forceinline__ Item decode_item(const Params& p, int item) {
+    Item w;
+    w.mt = item % p.m_tiles;
+    int r = item / p.m_tiles;
+    w.split = r % p.splits;
+    r /= p.splits;
+    w.nt = r % p.n_tiles;
+    w.z = r / p.n_tiles;
+    w.kc0 = w.split * p.chunks_per_split;
+    w.kc1 = min(p.K / BK, w.kc0 + p.chunks_per_split);
+    return w;
+}
+
+// Named barrier of the four epilogue warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// The same barrier, returning whether v held in every epilogue thread.
+__device__ __forceinline__ bool epi_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// One item's accumulator (TMEM columns 0..BN of `tacc`, this thread's lane
+// quarter already added) to global memory: bf16 rows of `out`, or this
+// split's fp32 rows of the partials.  Runs in the 128 epilogue threads
+// (t = 0..127, row = t in the tile); 32 columns per round through `stg`.
+__device__ __forceinline__ void store_tile(const Params& p, const Item& w, int Z, uint32_t tacc,
+                                           uint8_t* stg, int t, bool fp32) {
+    const int m0 = w.mt * BM, n0 = w.nt * p.BN;
+    const int n_valid = min(p.BN, p.N - n0);
+    const int mv = min(BM, p.M - m0);
+    float* stg_f = reinterpret_cast<float*>(stg);
+    uint16_t* stg_h = reinterpret_cast<uint16_t*>(stg);
+    for (int c0 = 0; c0 < n_valid; c0 += EPI_COLS) {
+        uint32_t r[32];
+        tmem_ld32(tacc + (uint32_t)c0, r);
+        if (fp32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) stg_f[j * BM + t] = __uint_as_float(r[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[j]));
+                stg_h[j * BM + t] = *reinterpret_cast<const uint16_t*>(&h);
+            }
+        }
+        epi_sync();
+        const int ncols = min(EPI_COLS, n_valid - c0);
+        if (fp32) {
+            float* base = p.ws_part + (((int64_t)w.split * Z + w.z) * p.N + n0 + c0) * p.M + m0;
+            for (int idx = t; idx < ncols * 32; idx += BM) {
+                const int j = idx >> 5, m = (idx & 31) * 4;
+                if (m < mv)
+                    *reinterpret_cast<float4*>(base + (int64_t)j * p.M + m) =
+                        *reinterpret_cast<const float4*>(stg_f + j * BM + m);
+            }
+        } else {
+            __nv_bfloat16* base = p.out + (int64_t)(n0 + c0) * p.ldo + (int64_t)w.z * p.out_z + m0;
+            for (int idx = t; idx < ncols * 16; idx += BM) {
+                const int j = idx >> 4, m = (idx & 15) * 8;
+                if (m >= mv) continue;
+                const uint4 v = *reinterpret_cast<const uint4*>(stg_h + j * BM + m);
+                __nv_bfloat16* dst = base + (int64_t)j * p.ldo + m;
+                if (p.vec_out) {
+                    *reinterpret_cast<uint4*>(dst) = v;
+                } else {
+                    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) reinterpret_cast<uint16_t*>(dst)[k] = e[k];
+                }
+            }
+        }
+        epi_sync();  // the staging buffer is rewritten by the next round
+    }
+}
+
+// The last CTA to finish a split tile adds every split's fp32 partial in
+// split order and writes the bf16 tile (128 epilogue threads).
+__device__ __forceinline__ void reduce_tile(const Params& p, const Item& w, int Z, int t) {
+    const int m0 = w.mt * BM, n0 = w.nt * p.BN;
+    const int n_valid = min(p.BN, p.N - n0);
+    const int mv = min(BM, p.M - m0);
+    const int64_t split_stride = (int64_t)Z * p.N * p.M;
+    const float* src0 = p.ws_part + ((int64_t)w.z * p.N + n0) * p.M + m0;
+    __nv_bfloat16* out0 = p.out + (int64_t)n0 * p.ldo + (int64_t)w.z * p.out_z + m0;
+    const int total = n_valid * 32;  // float4 pieces of the tile
+    for (int base = t; base < total; base += 4 * BM) {
+        float4 acc[4];
+        int64_t off[4];
+        bool on[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int idx = base + u * BM;
+            const int j = idx >> 5, m = (idx & 31) * 4;
+            on[u] = idx < total && m < mv;
+            off[u] = (int64_t)j * p.M + m;
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll 2
+        for (int s = 0; s < p.splits; ++s) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                v[u] = on[u] ? __ldcg(reinterpret_cast<const float4*>(src0 + s * split_stride + off[u]))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                acc[u].x += v[u].x;
+                acc[u].y += v[u].y;
+                acc[u].z += v[u].z;
+                acc[u].w += v[u].w;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (!on[u]) continue;
+            const int idx = base + u * BM;
+            const int j = idx >> 5, m = (idx & 31) * 4;
+            __nv_bfloat16* dst = out0 + (int64_t)j * p.ldo + m;
+            const uint32_t lo = pack2_bf16(acc[u].x, acc[u].y), hi = pack2_bf16(acc[u].z, acc[u].w);
+            if (p.vec_out) {
+                *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+            } else {
+                reinterpret_cast<uint16_t*>(dst)[0] = (uint16_t)lo;
+                reinterpret_cast<uint16_t*>(dst)[1] = (uint16_t)(lo >> 16);
+                reinterpret_cast<uint16_t*>(dst)[2] = (uint16_t)hi;
+                reinterpret_cast<uint16_t*>(dst)[3] = (uint16_t)(hi >> 16);
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
+             const __grid_constant__ CUtensorMap tm_x, const Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
-    const uint32_t xb = x_bytes(p.BN);
-    const uint32_t stage_bytes = A_BYTES + xb;  // multiple of 1024 (BN % 8 == 0)
+    const uint32_t xb = (uint32_t)p.BN * BK * 2;
+    const uint32_t stage_bytes = A_BYTES + xb;  // multiple of 1024 (BN % 16 == 0)
     const int S = p.stages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S * stage_bytes);
-    // bars[0..S): full, bars[S..2S): empty, bars[2S]: accumulator ready
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 1);
-    int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] abort, [1] skip, [2] reduce
+    uint8_t* stg = smem + S * stage_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stg + STG_BYTES);
+    // bars: [0, S) full, [S, 2S) empty, 2S + b acc_full, 2S + 2 + b acc_empty, 2S + 4 final
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+    int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] skip, [1] this tile's reducer
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int m_tile = blockIdx.x;
-    const int z = blockIdx.y / p.n_tiles;
-    const int n_tile = blockIdx.y % p.n_tiles;
-    const int split = blockIdx.z;
-    const int m0 = m_tile * BM, n0 = n_tile * p.BN;
-    const int kc0 = split * p.chunks_per_split;
-    const int kc1 = min(p.K / BK, kc0 + p.chunks_per_split);
-    uint32_t tmem_cols = 32;
-    while (tmem_cols < (uint32_t)p.BN) tmem_cols <<= 1;
+    const int i0 = (int)((int64_t)p.items * blockIdx.x / gridDim.x);
+    const int i1 = (int)((int64_t)p.items * (blockIdx.x + 1) / gridDim.x);
+    const int Z = p.items / (p.n_tiles * p.splits * p.m_tiles);
+    uint32_t acc_cols = 32;
+    while (acc_cols < (uint32_t)p.BN) acc_cols <<= 1;
+    const uint32_t tmem_cols = 2 * acc_cols;
 
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
-    const uint32_t acc_bar = smem_u32(bars + 2 * S);
+    const uint32_t accf0 = smem_u32(bars + 2 * S), acce0 = smem_u32(bars + 2 * S + 2);
+    const uint32_t fin = smem_u32(bars + 2 * S + 4);
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        mbar_init(acc_bar, 1);
-        flag[0] = 0;
-        flag[1] = device_status_raised() ? 1 : 0;  // one decision for the whole CTA
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf0 + 8 * b, 1);
+            mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
+        }
+        mbar_init(fin, 1);
+        flag[0] = device_status_raised() ? 1 : 0;  // one decision for the whole CTA
+        flag[1] = 0;
         fence_mbar_init_cluster();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_a2);
+        tma_prefetch_desc(&tm_x);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), tmem_cols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const bool skip = flag[1] != 0 || kc1 <= kc0;
+    const bool skip = flag[0] != 0;
 
-    bool ok = true;
-    if (!skip && warp == 0 && lane == 0) {
+    if (warp == 0) {
         // ---------------------------------------------------------- producer
-        const uint64_t pol = l2_policy_evict_first();
-        int it = 0;
-        for (int kc = kc0; kc < kc1; ++kc, ++it) {
-            const int s = it % S;
-            if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) { ok = false; break; }
-            const uint32_t sa = smem_u32(smem + s * stage_bytes);
-            const uint32_t sx = sa + A_BYTES;
-            mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
-            if (p.a_mn) {
-                tma_load_3d(sa, &tm_a, full0 + 8 * s, m0, kc * BK, z, pol);
-                tma_load_3d(sa + A_BYTES / 2, &tm_a, full0 + 8 * s, m0 + 64, kc * BK, z, pol);
-            } else {
-                tma_load_3d(sa, &tm_a, full0 + 8 * s, kc * BK, m0, z, pol);
+        if (!skip && lane == 0) {
+            const uint64_t pol_a = p.a_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int it = 0;
+            bool ok = true;
+            for (int item = i0; item < i1 && ok; ++item) {
+                const Item w = decode_item(p, item);
+                const bool second = w.mt >= p.m_split;
+                const CUtensorMap* am = second ? &tm_a2 : &tm_a;
+                const int m0 = (second ? w.mt - p.m_split : w.mt) * BM;
+                const int n0 = w.nt * p.BN;
+                for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
+                    const int s = it % S;
+                    if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) { ok = false; break; }
+                    const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                    const uint32_t sx = sa + A_BYTES;
+                    mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+                    if (p.a_mn) {
+                        tma_load_3d(sa, am, full0 + 8 * s, m0, kc * BK, w.z, pol_a);
+                        tma_load_3d(sa + A_BYTES / 2, am, full0 + 8 * s, m0 + 64, kc * BK, w.z, pol_a);
+                    } else {
+                        tma_load_3d(sa, am, full0 + 8 * s, kc * BK, m0, w.z, pol_a);
+                    }
+                    tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? w.z : 0, n0, pol_x);
+                }
             }
-            tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? z : 0, n0, pol);
+            // every issued copy lands before the CTA can exit (on the normal
+            // path these phases have completed; after an abort they may not)
+            for (int i = max(0, it - S); i < it; ++i)
+                mbar_wait_teardown(full0 + 8 * (i % S), (i / S) & 1, MLA_WAIT_LIMIT_NS);
         }
-        // every issued copy lands before the CTA can exit (on the normal path
-        // these phases have completed; after an abort they may not have)
-        for (int i = max(0, it - S); i < it; ++i)
-            mbar_wait_teardown(full0 + 8 * (i % S), (i / S) & 1, MLA_WAIT_LIMIT_NS);
-    } else if (!skip && warp == 1 && lane == 0) {
+    } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
-        const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
-        int it = 0;
-        for (int kc = kc0; kc < kc1; ++kc, ++it) {
-            const int s = it % S;
-            if (!mbar_wait(full0 + 8 * s, (it / S) & 1, 0x103)) { ok = false; break; }
-            tc_fence_after();
-            const uint32_t sa = smem_u32(smem + s * stage_bytes);
-            const uint32_t sx = sa + A_BYTES;
+        if (!skip) {
+            const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
+            int it = 0, acc = 0;
+            bool ok = true;
+            for (int item = i0; item < i1 && ok; ++item, ++acc) {
+                const Item w = decode_item(p, item);
+                const uint32_t b = acc & 1, use = acc >> 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(acce0 + 8 * b, (use & 1) ^ 1, 0x102));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t d = tmem + b * acc_cols;
+                for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
+                    const int s = it % S;
+                    ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (it / S) & 1, 0x103));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (elect_one_sync()) {
+                        const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                        const uint32_t sx = sa + A_BYTES;
 #pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk) {
-                // A: K-major 128B-swizzled rows of 64 k, +32 B per 16-k step;
-                //    MN-major: two 64-m boxes 8 KB apart, 16 k-rows = 2 KB.
-                const uint64_t da = p.a_mn ? smem_desc(sa + kk * 2048, 8192, 1024, SWZ_128B)
-                                           : smem_desc(sa + kk * 32, 16, 1024, SWZ_128B);
-                const uint64_t dx = smem_desc(sx + kk * 32, 16, 1024, SWZ_128B);
-                mma_ss(tmem, da, dx, idesc, (it > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < BK / 16; ++kk) {
+                            // A: K-major 128B-swizzled rows of 64 k, +32 B per 16-k step;
+                            //    MN-major: two 64-m boxes 8 KB apart, 16 k-rows = 2 KB.
+                            const uint64_t da = p.a_mn ? smem_desc(sa + kk * 2048, 8192, 1024, SWZ_128B)
+                                                       : smem_desc(sa + kk * 32, 16, 1024, SWZ_128B);
+                            const uint64_t dx = smem_desc(sx + kk * 32, 16, 1024, SWZ_128B);
+                            mma_ss(d, da, dx, idesc, (kc > w.kc0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc_commit(empty0 + 8 * s);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (elect_one_sync()) tc_commit(accf0 + 8 * b);
+                __syncwarp();
             }
-            tc_commit(empty0 + 8 * s);
-        }
-        tc_commit(acc_bar);  // also on the abort path: tracks every issued MMA
-    }
-    if (!ok) atomicExch(flag, 1);
-
-    // ------------------------------------------------------------- epilogue
-    // good: this CTA's accumulator is complete and no error is known
-    bool good = false;
-    if (!skip) {
-        good = __syncthreads_and(mbar_wait(acc_bar, 0, 0x104) ? 1 : 0) != 0;
-        tc_fence_after();
-        good = good && *flag == 0;
-    }
-    const int m = m0 + warp * 32 + lane;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-    const int n_valid = min(p.BN, p.N - n0);
-    if (p.splits == 1) {
-        if (good) {
-            __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
-            for (int c0 = 0; c0 < p.BN; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(trow + c0, r);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j < n_valid)
-                        dst[(int64_t)(n0 + c0 + j) * p.ldo] = __float2bfloat16_rn(__uint_as_float(r[j]));
-            }
+            // tracks every product issued, also on the abort path
+            if (elect_one_sync()) tc_commit(fin);
+            __syncwarp();
         }
     } else {
-        const int Z = gridDim.y / p.n_tiles;
-        if (good) {
-            float* part = p.ws_part + (((int64_t)split * Z + z) * p.N) * p.M + m;
-            for (int c0 = 0; c0 < p.BN; c0 += 16) {
-                uint32_t r[16];
-                tmem_ld16(trow + c0, r);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (c0 + j < n_valid) part[(int64_t)(n0 + c0 + j) * p.M] = __uint_as_float(r[j]);
-            }
-            __threadfence();
-        }
-        // Every CTA of the tile arrives on its counter -- also one that
-        // skipped or gave up -- and the last arrival resets it, so the
-        // counters are back at zero for the next call whatever happened in
-        // this one.  Only a last arrival that sees no error anywhere reduces.
-        __syncthreads();
-        const int tile = (z * p.n_tiles + n_tile) * (p.M / BM) + m_tile;
-        if (threadIdx.x == 0) {
-            const int prev = atomicAdd(p.ws_count + tile, 1);
-            const bool last = prev == p.splits - 1;
-            if (last) p.ws_count[tile] = 0;
-            flag[2] = last && good && !device_status_raised() ? 2 : 0;
-        }
-        __syncthreads();
-        if (flag[2] == 2) {  // last split of this tile: reduce in split order
-            __threadfence();
-            __nv_bfloat16* dst = p.out + (int64_t)z * p.out_z + m;
-            // 8 columns at a time, each split's 8 loads issued together (the
-            // sum still runs over the splits in order)
-            for (int nb = 0; nb < n_valid; nb += 8) {
-                float acc[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-#pragma unroll 4
-                for (int s = 0; s < p.splits; ++s) {
-                    const float* src = p.ws_part + (((int64_t)s * Z + z) * p.N + n0 + nb) * p.M + m;
-                    float v[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = nb + j < n_valid ? __ldcg(src + (int64_t)j * p.M) : 0.f;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[j] += v[j];
+        // ---------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int t = q * 32 + lane;  // row of the tile this thread reads from TMEM
+        bool ok = !skip;
+        int acc = 0;
+        for (int item = i0; item < i1; ++item, ++acc) {
+            const Item w = decode_item(p, item);
+            const uint32_t b = acc & 1, use = acc >> 1;
+            bool good = ok && __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * b, use & 1, 0x104));
+            good = epi_sync_and(good);
+            ok = good;
+            tc_fence_after();
+            if (good)
+                store_tile(p, w, Z, tmem + b * acc_cols + ((uint32_t)(q * 32) << 16), stg, t,
+                           p.mode != OUT_BF16);
+            // the buffer is free for the item after next once this warp's reads are done
+            tc_fence_before();
+            __syncwarp();
+            if (good && lane == 0) mbar_arrive(acce0 + 8 * b);
+            if (p.mode == OUT_REDUCE) {
+                // Every CTA of a split tile arrives on its counter -- also one
+                // that skipped or gave up -- and the last arrival resets it, so
+                // the counters are back at zero for the next call whatever
+                // happened in this one.  Only a last arrival that sees no error
+                // anywhere reduces.
+                __threadfence();
+                epi_sync();
+                if (t == 0) {
+                    const int tile = (w.z * p.n_tiles + w.nt) * p.m_tiles + w.mt;
+                    const int prev = atomicAdd(p.ws_count + tile, 1);
+                    const bool last = prev == p.splits - 1;
+                    if (last) p.ws_count[tile] = 0;
+                    flag[1] = last && good && !device_status_raised() ? 1 : 0;
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    if (nb + j < n_valid) dst[(int64_t)(n0 + nb + j) * p.ldo] = __float2bfloat16_rn(acc[j]);
+                epi_sync();
+                if (flag[1]) {
+                    __threadfence();
+                    reduce_tile(p, w, Z, t);
+                }
             }
         }
     }
+
     // the products (and their commits) are done before TMEM goes away, even
     // when the epilogue gave up waiting for them
-    if (!skip && threadIdx.x == 32) mbar_wait_teardown(acc_bar, 0, MLA_WAIT_LIMIT_NS);
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) tmem_dealloc(tmem, tmem_cols);
+    tc_fence_after();
+    if (warp == 1) {
+        if (!skip) mbar_wait_teardown(fin, 0, MLA_WAIT_LIMIT_NS);
+        __syncwarp();
+        tmem_dealloc(tmem, tmem_cols);
+    }
 }
 
 }  // namespace gemm

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -90,7 +91,7 @@ bool device_info(DeviceInfo& out) {
                                  (int)mla::dec::SMEM_ALLOC) != cudaSuccess)
             return false;
         if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 200 * 1024) != cudaSuccess)
+                                 (int)mla::gemm::SMEM_CAP) != cudaSuccess)
             return false;
         if (cudaFuncSetAttribute(mla::pre::prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::pre::SMEM_ALLOC) != cudaSuccess)
@@ -175,91 +176,142 @@ DecodeWs decode_ws_layout(int64_t U, int64_t G, int d_c) {
 // ------------------------------------------------------------- GEMM plan
 
 struct GemmPlan {
-    int BN, n_tiles, splits, chunks;
-    size_t ws_part_bytes, ws_count_bytes;
+    int BN = 16, n_tiles = 1, m_tiles = 1, splits = 1, chunks = 1, items = 0, grid = 0, stages = 1;
+    int mode = mla::gemm::OUT_BF16;
+    size_t smem = 0, ws_part_bytes = 0, ws_count_bytes = 0;
 };
 
-// max_splits > 0 caps the split-K factor: the last CTA of a tile adds the
-// splits' partials serially, so a GEMM with few output tiles (a small M)
-// would otherwise spend longer reducing than streaming its weight.
-GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, bool allow_split, int max_splits = 0) {
+enum SplitMode : int { kNoSplit = 0, kSplitReduce = 1, kSplitParts = 2 };
+
+// The GEMM's work plan for D [M x N] per head z (M rows that exist, a
+// multiple of 8) with reduction length K.  One CTA per SM walks a
+// contiguous range of items; the K split is chosen by a cost in units of one
+// A chunk (16 KB): the larger of the evenly shared stream (all tiles' chunks
+// over the SMs) and the busiest CTA's chunks at twice the fair per-SM rate,
+// plus the fp32 partials each split writes and the reduction reads.
+GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max_splits = 64) {
     GemmPlan g;
     g.BN = N >= 256 ? 256 : ((N + 15) / 16) * 16;
     g.n_tiles = (N + g.BN - 1) / g.BN;
-    const int chunks_total = K / mla::gemm::BK;
-    const int tiles = (M / mla::gemm::BM) * Z * g.n_tiles;
-    int splits = 1;
-    if (allow_split) {
-        const int target = 2 * sms;  // two CTAs fit per SM
-        splits = (target + tiles / 2) / tiles;
-        if (splits < 1) splits = 1;
-        if (splits > chunks_total) splits = chunks_total;
-        if (max_splits > 0 && splits > max_splits) splits = max_splits;
+    g.m_tiles = (M + mla::gemm::BM - 1) / mla::gemm::BM;
+    const int kc = K / mla::gemm::BK;
+    const int64_t tiles = (int64_t)Z * g.m_tiles * g.n_tiles;
+    const double epi = g.BN / 32.0;  // an fp32 partial tile, in A chunks
+    double best = 1e300;
+    int best_s = 1;
+    const int s_max = split == kNoSplit ? 1 : std::max(1, std::min(kc, max_splits));
+    for (int s = 1; s <= s_max; ++s) {
+        const int cps = (kc + s - 1) / s;
+        if ((kc + cps - 1) / cps != s) continue;  // the same cut as a smaller s
+        const int64_t items = tiles * s;
+        const int64_t G = std::min<int64_t>(items, sms);
+        const int64_t per = (items + G - 1) / G;
+        double cost = std::max((double)tiles * kc / sms, (double)per * cps / 2.0);
+        if (split == kSplitParts) cost += 0.5 * per * epi;
+        else if (s > 1) cost += 0.5 * per * epi + 0.25 * s * epi;
+        if (cost < best - 1e-9) {
+            best = cost;
+            best_s = s;
+        }
     }
-    g.chunks = (chunks_total + splits - 1) / splits;
-    g.splits = (chunks_total + g.chunks - 1) / g.chunks;
-    g.ws_part_bytes = g.splits > 1 ? sizeof(float) * (size_t)g.splits * Z * N * M : 0;
-    g.ws_count_bytes = g.splits > 1 ? sizeof(int) * (size_t)tiles : 0;
+    g.chunks = (kc + best_s - 1) / best_s;
+    g.splits = (kc + g.chunks - 1) / g.chunks;
+    g.mode = split == kSplitParts ? mla::gemm::OUT_PARTS
+                                  : (g.splits > 1 ? mla::gemm::OUT_REDUCE : mla::gemm::OUT_BF16);
+    const int64_t items = tiles * g.splits;
+    g.items = items > 0x7FFFFFFF ? 0 : (int)items;  // 0: too large (refused by the caller)
+    g.grid = (int)std::min<int64_t>(items, sms);
+    const size_t stage = (size_t)mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
+    const size_t fixed = 1024 + mla::gemm::STG_BYTES + 256;
+    g.stages = (int)std::min<size_t>(mla::gemm::MAX_STAGES, (mla::gemm::SMEM_CAP - fixed) / stage);
+    g.smem = fixed + (size_t)g.stages * stage;
+    g.ws_part_bytes = g.mode != mla::gemm::OUT_BF16 ? sizeof(float) * (size_t)g.splits * Z * N * M : 0;
+    g.ws_count_bytes = g.mode == mla::gemm::OUT_REDUCE ? sizeof(int) * (size_t)tiles : 0;
     return g;
 }
 
-mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tx, int M, int N, int K, int Z,
-                         int a_mn, int x_batched, const GemmPlan& g, __nv_bfloat16* out,
-                         int64_t ldo, int64_t out_z, float* ws_part, int* ws_count,
+// Launch the persistent GEMM.  ta2 serves the M tiles from m_split on (pass
+// ta and m_split = m_tiles when there is one A map).
+mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_split, const CUtensorMap& tx,
+                         int M, int N, int K, int Z, int a_mn, int x_batched, const GemmPlan& g,
+                         __nv_bfloat16* out, int64_t ldo, int64_t out_z, float* ws_part, int* ws_count,
                          cudaStream_t st) {
+    if (g.items < 1 || M % 8 != 0) return MLA_ERR_UNSUPPORTED;
+    if (g.mode != mla::gemm::OUT_BF16 && (!ws_part || !aligned16(ws_part))) return MLA_ERR_INVALID_ARG;
+    if (g.mode == mla::gemm::OUT_REDUCE && !ws_count) return MLA_ERR_INVALID_ARG;
     mla::gemm::Params p;
     p.M = M;
     p.N = N;
     p.K = K;
+    p.m_tiles = g.m_tiles;
+    p.m_split = m_split;
     p.BN = g.BN;
     p.n_tiles = g.n_tiles;
     p.a_mn = a_mn;
     p.x_batched = x_batched;
     p.splits = g.splits;
     p.chunks_per_split = g.chunks;
-    p.stages = g.chunks < mla::gemm::STAGES ? (g.chunks > 0 ? g.chunks : 1) : mla::gemm::STAGES;
+    p.items = g.items;
+    p.stages = g.stages;
+    p.mode = g.mode;
+    p.a_evict_first = g.n_tiles == 1 ? 1 : 0;
+    p.vec_out = (aligned16(out) && ldo % 8 == 0 && out_z % 8 == 0) ? 1 : 0;
     p.out = out;
     p.ldo = ldo;
     p.out_z = out_z;
     p.ws_part = ws_part;
     p.ws_count = ws_count;
-    const size_t smem = (size_t)p.stages * (mla::gemm::A_BYTES + g.BN * mla::gemm::BK * 2) + 256 + 1024;
-    dim3 grid(M / mla::gemm::BM, Z * g.n_tiles, g.splits);
-    mla::gemm::wgemm_kernel<<<grid, mla::gemm::THREADS, smem, st>>>(ta, tx, p);
+    (void)Z;
+    mla::gemm::wgemm_kernel<<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
     return launch_status();
 }
 
-size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& tx, int M, int N, int K, int Z,
+                         int a_mn, int x_batched, const GemmPlan& g, __nv_bfloat16* out, int64_t ldo,
+                         int64_t out_z, float* ws_part, int* ws_count, cudaStream_t st) {
+    return launch_gemm(ta, ta, g.m_tiles, tx, M, N, K, Z, a_mn, x_batched, g, out, ldo, out_z, ws_part,
+                       ws_count, st);
+}
 
-// Split-K cap of the prologue's GEMMs (W^DKV h has only d_c / 128 output
-// tiles per token block).
-constexpr int kPrologueMaxSplits = 8;
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Scratch of one plain GEMM: split-K partials, then the arrival counters
 // (zero before the first use; every call leaves them at zero).
 size_t plain_gemm_ws_bytes(const GemmPlan& g) { return round256(g.ws_part_bytes) + g.ws_count_bytes; }
 
-// out[n * ldo + m] = sum_k W[m, k] X[n, k] in bf16: the weight W [M, K]
-// (K-major) on the UMMA M axis, the activation rows X [N, K] on N.
-// X's rows are x_ld elements apart (0: K).
+float* ws_parts(const GemmPlan& g, void* ws) {
+    return g.mode != mla::gemm::OUT_BF16 ? static_cast<float*>(ws) : nullptr;
+}
+int* ws_counts(const GemmPlan& g, void* ws) {
+    return g.mode == mla::gemm::OUT_REDUCE
+               ? reinterpret_cast<int*>(static_cast<char*>(ws) + round256(g.ws_part_bytes))
+               : nullptr;
+}
+
+// Tensor maps of a K-major weight W [M, K] (A operand, 128 x 64 boxes) and
+// of activation rows X [N, K] with rows x_ld elements apart (BN x 64 boxes).
+bool weight_map(CUtensorMap* m, const void* W, int M, int K) {
+    cuuint64_t ad[3] = {(cuuint64_t)K, (cuuint64_t)M, 1};
+    cuuint64_t as[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * M * 2};
+    cuuint32_t ab[3] = {64, 128, 1};
+    return make_map(m, W, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+bool rows_map(CUtensorMap* m, const void* X, int N, int K, int64_t x_ld, int BN) {
+    cuuint64_t xd[3] = {(cuuint64_t)K, 1, (cuuint64_t)N};
+    cuuint64_t xs[2] = {(cuuint64_t)x_ld * 2, (cuuint64_t)x_ld * 2};
+    cuuint32_t xbx[3] = {64, 1, (cuuint32_t)BN};
+    return make_map(m, X, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// out[n * ldo + m] = sum_k W[m, k] X[n, k] in bf16 (or the fp32 partials of
+// g's mode): the weight W [M, K] (K-major) on the UMMA M axis, the
+// activation rows X [N, K] on N.  X's rows are x_ld elements apart (0: K).
 mla_status_t plain_gemm(const void* W, const void* X, __nv_bfloat16* out, int64_t ldo, int M, int N,
                         int K, const GemmPlan& g, void* ws, cudaStream_t st, int64_t x_ld = 0) {
     CUtensorMap ta, tx;
     if (x_ld == 0) x_ld = K;
-    cuuint64_t ad[3] = {(cuuint64_t)K, (cuuint64_t)M, 1};
-    cuuint64_t as[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * M * 2};
-    cuuint32_t ab[3] = {64, 128, 1};
-    cuuint64_t xd[3] = {(cuuint64_t)K, 1, (cuuint64_t)N};
-    cuuint64_t xs[2] = {(cuuint64_t)x_ld * 2, (cuuint64_t)x_ld * 2};
-    cuuint32_t xbx[3] = {64, 1, (cuuint32_t)g.BN};
-    if (!make_map(&ta, W, 3, ad, as, ab, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tx, X, 3, xd, xs, xbx, CU_TENSOR_MAP_SWIZZLE_128B))
-        return MLA_ERR_CUDA;
-    float* ws_part = g.splits > 1 ? static_cast<float*>(ws) : nullptr;
-    int* ws_count = g.splits > 1
-                        ? reinterpret_cast<int*>(static_cast<char*>(ws) + round256(g.ws_part_bytes))
-                        : nullptr;
-    return launch_gemm(ta, tx, M, N, K, 1, 0, 0, g, out, ldo, 0, ws_part, ws_count, st);
+    if (!weight_map(&ta, W, M, K) || !rows_map(&tx, X, N, K, x_ld, g.BN)) return MLA_ERR_CUDA;
+    return launch_gemm(ta, tx, M, N, K, 1, 0, 0, g, out, ldo, 0, ws_parts(g, ws), ws_counts(g, ws), st);
 }
 
 }  // namespace
@@ -331,8 +383,7 @@ mla_status_t mla_absorb_q(const void* q_nope, const void* w_uk, void* q_lat, int
     if (d_c % 128 != 0 || d_h % 64 != 0 || H > 65535) return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan(d_c, rows, d_h, H, di.sms, false);
-    if ((int64_t)H * g.n_tiles > 65535) return MLA_ERR_UNSUPPORTED;  // grid.y
+    const GemmPlan g = gemm_plan(d_c, rows, d_h, H, di.sms, kNoSplit);
     // A = W^UK_i^T, stored along d_c: MN-major tiles [64 d_h rows x 64 d_c]
     CUtensorMap ta, tx;
     cuuint64_t ad[3] = {(cuuint64_t)d_c, (cuuint64_t)d_h, (cuuint64_t)H};
@@ -354,8 +405,8 @@ size_t mla_out_proj_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t 
     if (dtype != MLA_BF16 || rows < 1 || H < 1 || d_h < 1 || d < 128) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    const GemmPlan g = gemm_plan(d, rows, H * d_h, 1, di.sms, true);
-    return ((g.ws_part_bytes + 255) & ~size_t(255)) + g.ws_count_bytes;
+    const GemmPlan g = gemm_plan(d, rows, H * d_h, 1, di.sms, kSplitReduce);
+    return plain_gemm_ws_bytes(g);
 }
 
 mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void* v_tmp, void* out,
@@ -382,11 +433,10 @@ mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
     const int K2 = H * d_h;
-    const GemmPlan g1 = gemm_plan(d_h, rows, d_c, H, di.sms, false);
-    const GemmPlan g2 = gemm_plan(d, rows, K2, 1, di.sms, true);
-    const size_t part_bytes = (g2.ws_part_bytes + 255) & ~size_t(255);
-    if (g2.splits > 1 && (!workspace || workspace_bytes < part_bytes + g2.ws_count_bytes ||
-                          !aligned16(workspace)))
+    const GemmPlan g1 = gemm_plan(d_h, rows, d_c, H, di.sms, kNoSplit);
+    const GemmPlan g2 = gemm_plan(d, rows, K2, 1, di.sms, kSplitReduce);
+    if (g2.mode != mla::gemm::OUT_BF16 &&
+        (!workspace || workspace_bytes < plain_gemm_ws_bytes(g2) || !aligned16(workspace)))
         return MLA_ERR_INVALID_ARG;
     CUtensorMap ta1, tx1, ta2, tx2;
     {   // v = W^UV_i o_i : A K-major [d_h rows x 64 d_c], X = o [rows, H, d_c]
@@ -415,10 +465,8 @@ mla_status_t mla_out_proj(const void* o, const void* w_uv, const void* w_o, void
                                  static_cast<__nv_bfloat16*>(v_tmp), (int64_t)K2, d_h, nullptr,
                                  nullptr, st);
     if (s != MLA_OK) return s;
-    float* ws_part = static_cast<float*>(workspace);
-    int* ws_count = reinterpret_cast<int*>(static_cast<char*>(workspace) + part_bytes);
     return launch_gemm(ta2, tx2, d, rows, K2, 1, 0, 0, g2, static_cast<__nv_bfloat16*>(out), d, 0,
-                       g2.splits > 1 ? ws_part : nullptr, g2.splits > 1 ? ws_count : nullptr, st);
+                       ws_parts(g2, workspace), ws_counts(g2, workspace), st);
 }
 
 // ------------------------------------------------- merged output weight
@@ -484,7 +532,7 @@ mla_status_t mla_absorb_q_merged(const void* c_q, const void* w_merged, void* q_
     if (!device_info(di)) return MLA_ERR_CUDA;
     // q_lat = W_merged c^Q: the folded weight [d_q, H * d_c] is stored along
     // its output axis, so it is an MN-major A operand of the GEMM
-    const GemmPlan g = gemm_plan((int)M, rows, d_q, 1, di.sms, false);
+    const GemmPlan g = gemm_plan((int)M, rows, d_q, 1, di.sms, kNoSplit);
     CUtensorMap ta, tx;
     cuuint64_t ad[3] = {(cuuint64_t)M, (cuuint64_t)d_q, 1};
     cuuint64_t as[2] = {(cuuint64_t)M * 2, (cuuint64_t)M * d_q * 2};
@@ -505,7 +553,7 @@ size_t mla_out_proj_merged_workspace_size(int rows, int H, int d_c, int d, mla_d
     if (K > (1 << 30)) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, true));
+    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, kSplitReduce));
 }
 
 mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out, int rows, int H,
@@ -528,8 +576,8 @@ mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out,
     if (d % 128 != 0 || d_c % 64 != 0) return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, true);
-    if (g.splits > 1 &&
+    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, kSplitReduce);
+    if (g.mode != mla::gemm::OUT_BF16 &&
         (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g)))
         return MLA_ERR_INVALID_ARG;
     // out = W_merged o on the tensor cores: the merged weight on the UMMA M
@@ -540,12 +588,34 @@ mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out,
 
 // ------------------------------------------- mla_cache_append / mla_project_q
 
+// RoPE frequencies f_k = base^(-2k/d_r) / 2pi as 0.64 fixed-point fractions
+// of a turn (the kernels multiply them by the position modulo 2^64), taken
+// in extended precision on the host.
+bool rope_freqs(uint64_t (&f)[mla::pro::MAX_PAIRS], int d_r, double base) {
+    if (d_r < 2 || d_r / 2 > mla::pro::MAX_PAIRS || !(base > 0.0)) return false;
+    const long double two_pi = 6.283185307179586476925286766559005768L;
+    for (int k = 0; k < mla::pro::MAX_PAIRS; ++k) f[k] = 0;
+    for (int k = 0; k < d_r / 2; ++k) {
+        long double fr = powl((long double)base, -2.0L * k / (long double)d_r) / two_pi;
+        fr -= floorl(fr);
+        const long double v = ldexpl(fr, 64);
+        f[k] = v >= 18446744073709551615.0L ? ~0ull : (uint64_t)v;
+    }
+    return true;
+}
+
+// The cache write's GEMM covers [W^DKV ; W^KR] as M = d_c + d_r rows; its
+// plan (and so the workspace) depends on d_r only through the number of M
+// tiles, which is d_c / 128 + 1 for every d_r <= 128.
+GemmPlan cache_append_plan(int N, int d, int d_c, int d_r, int sms) {
+    return gemm_plan(d_c + d_r, N, d, 1, sms, kSplitParts);
+}
+
 size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype) {
     if (dtype != MLA_BF16 || N < 1 || d < 64 || d_c < 128) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    const GemmPlan g = gemm_plan(d_c, N, d, 1, di.sms, true, kPrologueMaxSplits);
-    return round256(sizeof(__nv_bfloat16) * (size_t)N * d_c) + plain_gemm_ws_bytes(g);
+    return plain_gemm_ws_bytes(cache_append_plan(N, d, d_c, 2 * mla::pro::MAX_PAIRS, di.sms));
 }
 
 mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr,
@@ -563,13 +633,14 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
     if (!aligned16(h) || !aligned16(w_dkv) || !aligned16(w_kr) || !aligned16(kv_pool))
         return MLA_ERR_INVALID_ARG;
     if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
-    if (d_c % 2 != 0) return MLA_ERR_UNSUPPORTED;  // the kernels' row tiles keep RoPE pairs whole
+    if (d_c % 2 != 0 || d_r > 2 * mla::pro::MAX_PAIRS) return MLA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     mla::pro::KvParams p;
     p.h = h;
     p.w_dkv = w_dkv;
     p.w_kr = w_kr;
-    p.c_tmp = nullptr;
+    p.parts = nullptr;
+    p.splits = 0;
     p.seq_ids = seq_ids;
     p.positions = positions;
     p.page_table = page_table;
@@ -582,32 +653,37 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
     p.page = page_size;
     p.max_pages = max_pages;
     p.num_pages = num_pages;
-    p.rope_base = rope_base;
-    const unsigned gx = (unsigned)((N + mla::pro::TOK - 1) / mla::pro::TOK);
+    if (!rope_freqs(p.freq, d_r, rope_base)) return MLA_ERR_INVALID_ARG;
     if (dtype == MLA_FP32) {
         if (d % 4 != 0) return MLA_ERR_UNSUPPORTED;
-        p.e_first = 0;
-        const dim3 grid(gx, (unsigned)((d_c + d_r + mla::pro::ROWS - 1) / mla::pro::ROWS));
-        mla::pro::kv_rows_kernel<float><<<grid, mla::pro::THREADS, 0, st>>>(p);
+        const dim3 grid((unsigned)((N + mla::pro::TOK - 1) / mla::pro::TOK),
+                        (unsigned)((d_c + d_r + mla::pro::ROWS - 1) / mla::pro::ROWS));
+        mla::pro::kv_rows_fp32_kernel<<<grid, mla::pro::THREADS, 0, st>>>(p);
         return launch_status();
     }
     if (d_c % 128 != 0 || d % 64 != 0 || d_r % 8 != 0) return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan(d_c, N, d, 1, di.sms, true, kPrologueMaxSplits);
-    const size_t c_bytes = round256(sizeof(__nv_bfloat16) * (size_t)N * d_c);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < c_bytes + plain_gemm_ws_bytes(g))
+    const GemmPlan g = cache_append_plan(N, d, d_c, d_r, di.sms);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g))
         return MLA_ERR_INVALID_ARG;
-    // c = W^DKV h on the tensor cores into the workspace, then W^KR h, the
-    // rotation and the scatter of whole rows into the pool
-    __nv_bfloat16* c_tmp = static_cast<__nv_bfloat16*>(workspace);
-    mla_status_t s = plain_gemm(w_dkv, h, c_tmp, d_c, d_c, N, d, g,
-                                static_cast<char*>(workspace) + c_bytes, st);
+    // [W^DKV ; W^KR] h on the tensor cores: M tiles 0 .. d_c/128 - 1 from
+    // W^DKV, the last from W^KR (its rows past d_r read as zeros), each K
+    // split's fp32 partial into the workspace; then the finishing kernel
+    // adds the splits, rotates k^R and writes whole pool rows.
+    CUtensorMap ta, ta2, tx;
+    if (!weight_map(&ta, w_dkv, d_c, d) || !weight_map(&ta2, w_kr, d_r, d) ||
+        !rows_map(&tx, h, N, d, d, g.BN))
+        return MLA_ERR_CUDA;
+    float* parts = ws_parts(g, workspace);
+    mla_status_t s = launch_gemm(ta, ta2, d_c / mla::gemm::BM, tx, d_c + d_r, N, d, 1, 0, 0, g, nullptr, 0,
+                                 0, parts, nullptr, st);
     if (s != MLA_OK) return s;
-    p.c_tmp = c_tmp;
-    p.e_first = d_c;
-    const dim3 grid(gx, (unsigned)((d_r + mla::pro::ROWS - 1) / mla::pro::ROWS));
-    mla::pro::kv_rows_kernel<__nv_bfloat16><<<grid, mla::pro::THREADS, 0, st>>>(p);
+    p.parts = parts;
+    p.splits = g.splits;
+    const unsigned threads = (unsigned)(((d_c + d_r) / 2 + 31) / 32 * 32);
+    if (threads > 1024) return MLA_ERR_UNSUPPORTED;
+    mla::pro::kv_finish_bf16_kernel<<<(unsigned)N, threads, 0, st>>>(p);
     return launch_status();
 }
 
@@ -617,8 +693,7 @@ size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_d
     if (M % 128 != 0 || M > (1 << 30)) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, true, kPrologueMaxSplits);
-    return round256(sizeof(__nv_bfloat16) * (size_t)N * (size_t)M) + plain_gemm_ws_bytes(g);
+    return plain_gemm_ws_bytes(gemm_plan((int)M, N, d, 1, di.sms, kSplitParts));
 }
 
 mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
@@ -632,14 +707,15 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
     if (!aligned16(h) || !aligned16(w_q) || !aligned16(q_nope) || !aligned16(q_pe))
         return MLA_ERR_INVALID_ARG;
     if (dtype != MLA_BF16 && dtype != MLA_FP32) return MLA_ERR_INVALID_ARG;
-    if (d_h % 2 != 0) return MLA_ERR_UNSUPPORTED;  // the kernels' row tiles keep RoPE pairs whole
+    if (d_h % 2 != 0 || d_r > 2 * mla::pro::MAX_PAIRS) return MLA_ERR_UNSUPPORTED;
     const int64_t M = (int64_t)H * (d_h + d_r);
     if (M > (1 << 30)) return MLA_ERR_UNSUPPORTED;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     mla::pro::QParams p;
     p.h = h;
     p.w_q = w_q;
-    p.q_tmp = nullptr;
+    p.parts = nullptr;
+    p.splits = 0;
     p.positions = positions;
     p.q_nope = q_nope;
     p.q_pe = q_pe;
@@ -648,7 +724,7 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
     p.H = H;
     p.d_h = d_h;
     p.d_r = d_r;
-    p.rope_base = rope_base;
+    if (!rope_freqs(p.freq, d_r, rope_base)) return MLA_ERR_INVALID_ARG;
     if (dtype == MLA_FP32) {
         const int64_t gy = (M + mla::pro::ROWS - 1) / mla::pro::ROWS;
         if (d % 4 != 0 || gy > 65535) return MLA_ERR_UNSUPPORTED;
@@ -656,22 +732,24 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
         mla::pro::q_rows_fp32_kernel<<<grid, mla::pro::THREADS, 0, st>>>(p);
         return launch_status();
     }
-    if (M % 128 != 0 || d % 64 != 0 || d_h % 8 != 0 || d_r % 8 != 0 || d_r > 8192)
+    if (M % 128 != 0 || d % 64 != 0 || d_h % 8 != 0 || d_r % 8 != 0) return MLA_ERR_UNSUPPORTED;
+    const int threads = mla::pro::Q_HEADS * (d_h + d_r) / 2;
+    if (threads > 1024 || (H + mla::pro::Q_HEADS - 1) / mla::pro::Q_HEADS > 65535)
         return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, true, kPrologueMaxSplits);
-    const size_t q_bytes = round256(sizeof(__nv_bfloat16) * (size_t)N * (size_t)M);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < q_bytes + plain_gemm_ws_bytes(g))
+    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, kSplitParts);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g))
         return MLA_ERR_INVALID_ARG;
-    // q = W^Q h on the tensor cores into the workspace, then the split per
-    // head and the rotation of the RoPE part
-    __nv_bfloat16* q_tmp = static_cast<__nv_bfloat16*>(workspace);
-    mla_status_t s = plain_gemm(w_q, h, q_tmp, M, (int)M, N, d, g,
-                                static_cast<char*>(workspace) + q_bytes, st);
+    // W^Q h on the tensor cores, each K split's fp32 partial into the
+    // workspace; then the finishing kernel adds the splits, splits each row
+    // per head, rotates q^R and rounds once
+    mla_status_t s = plain_gemm(w_q, h, nullptr, 0, (int)M, N, d, g, workspace, st);
     if (s != MLA_OK) return s;
-    p.q_tmp = q_tmp;
-    mla::pro::q_split_bf16_kernel<<<(unsigned)N, mla::pro::THREADS, sizeof(float) * (size_t)d_r, st>>>(p);
+    p.parts = ws_parts(g, workspace);
+    p.splits = g.splits;
+    const dim3 grid((unsigned)N, (unsigned)((H + mla::pro::Q_HEADS - 1) / mla::pro::Q_HEADS));
+    mla::pro::q_finish_bf16_kernel<<<grid, (unsigned)threads, 0, st>>>(p);
     return launch_status();
 }
 
@@ -683,7 +761,7 @@ size_t mla_prefill_workspace_size(int rows, int H, int d_h, int d, mla_dtype_t d
     if (K > (1 << 30)) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, true));
+    return plain_gemm_ws_bytes(gemm_plan(d, rows, (int)K, 1, di.sms, kSplitReduce));
 }
 
 mla_status_t mla_prefill_expand(const void* kv, const void* w_uk, const void* w_uv, void* k_nope,
@@ -703,7 +781,7 @@ mla_status_t mla_prefill_expand(const void* kv, const void* w_uk, const void* w_
     // K_nope[r, i, :] = W^UK_i c_r and V[r, i, :] = W^UV_i c_r: the stacked
     // [H * d_h x d_c] weight on the UMMA M axis, the latents c (the first d_c
     // values of each cache row) on N, no split of the short reduction
-    const GemmPlan g = gemm_plan((int)M, rows, d_c, 1, di.sms, false);
+    const GemmPlan g = gemm_plan((int)M, rows, d_c, 1, di.sms, kNoSplit);
     mla_status_t s = plain_gemm(w_uk, kv, static_cast<__nv_bfloat16*>(k_nope), M, (int)M, rows, d_c, g,
                                 nullptr, st, d_c + d_r);
     if (s != MLA_OK) return s;
@@ -771,8 +849,9 @@ mla_status_t mla_prefill_out(const void* u, const void* w_o, void* out, int rows
     if (d % 128 != 0 || K % 64 != 0 || K > (1 << 30)) return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, true);
-    if (g.splits > 1 && (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g)))
+    const GemmPlan g = gemm_plan(d, rows, (int)K, 1, di.sms, kSplitReduce);
+    if (g.mode != mla::gemm::OUT_BF16 &&
+        (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g)))
         return MLA_ERR_INVALID_ARG;
     // out = W^O u: W^O [d x H * d_h] on the UMMA M axis, the rows of u on N
     return plain_gemm(w_o, u, static_cast<__nv_bfloat16*>(out), d, d, rows, (int)K, g, workspace,
