@@ -11,15 +11,20 @@
 // 128 x 64 tiles, K-major or MN-major (W^UK, whose stored rows run along
 // d_c); X is K-major, BN rows x 64 per stage.
 //
-// Work is cut into items (head z, N tile, K split, M tile), M tile fastest.
-// One CTA per SM walks a contiguous range of items with one continuous TMA
-// ring, so the copies of the next item start while the current one is still
-// being multiplied, and the accumulator is double-buffered in TMEM so the
-// epilogue of item i runs while the products of item i+1 are issued.
+// Work is cut into items (head z, N tile, K split, M unit of MT = 1 or 2
+// M tiles), M unit fastest.  With MT = 2 the two A tiles of a stage share
+// one X tile: the TMA unit issues about one 128-byte row per 3 cycles per
+// SM (measured), so halving the X rows per A byte raises what one SM can
+// stream.  One CTA per SM walks a contiguous range of items with one
+// continuous TMA ring, so the copies of the next item start while the
+// current one is still being multiplied, and the accumulator is
+// double-buffered in TMEM so the epilogue of item i runs while the products
+// of item i+1 are issued; the epilogue hands its TMEM buffer back as soon as
+// the columns are in registers, before its stores.
 //
 // Roles (192 threads): warp 0 (one lane) issues TMA; warp 1 owns TMEM and
 // issues UMMA from an elected lane; warps 2..5 run the epilogue, warp w
-// reading TMEM lanes 32 (w % 4) .. +31.  The epilogue stages 32 accumulator
+// reading TMEM lanes 32 (w % 4) .. +31.  The epilogue stages 64 accumulator
 // columns at a time through shared memory, so that every global store is a
 // 16-byte piece of a contiguous output row.
 //
@@ -46,8 +51,8 @@ constexpr int MAX_STAGES = 8;
 constexpr int THREADS = 192;
 constexpr int EPI_WARP0 = 2;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB per stage
-constexpr int EPI_COLS = 32;                    // accumulator columns staged per round
-constexpr int STG_BYTES = EPI_COLS * BM * 4;    // 16 KB (fp32 rows of 128)
+constexpr int EPI_COLS = 64;                    // accumulator columns staged per round
+constexpr int STG_BYTES = EPI_COLS * BM * 4;    // 32 KB (fp32 rows of 128)
 constexpr uint32_t SMEM_CAP = 227 * 1024;
 
 enum : int { OUT_BF16 = 0, OUT_REDUCE = 1, OUT_PARTS = 2 };
@@ -56,13 +61,15 @@ struct Params {
     int M;                // rows of D that exist (a multiple of 8; the last M tile may be partial)
     int N, K;             // columns of D; reduction length (a multiple of BK)
     int m_tiles;          // ceil(M / BM)
+    int MT;               // M tiles per item (1, or 2 sharing each X tile)
+    int m_units;          // m_tiles / MT
     int m_split;          // M tiles >= m_split load A from the second map, at row (mt - m_split) * BM
     int BN, n_tiles;      // N tile (multiple of 16, <= 256) and ceil(N / BN)
     int a_mn;             // A stored MN-major
     int x_batched;        // X has a head coordinate (z); else z = 0 for X
     int splits;           // K splits
     int chunks_per_split; // K chunks (of BK) per split; the last split may be shorter
-    int items;            // Z * n_tiles * splits * m_tiles
+    int items;            // Z * n_tiles * splits * m_units
     int stages;           // TMA ring depth, 1..MAX_STAGES
     int mode;             // OUT_BF16 / OUT_REDUCE / OUT_PARTS
     int a_evict_first;    // A is read once (one N tile): let it leave L2 first
@@ -74,13 +81,13 @@ struct Params {
 };
 
 struct Item {
-    int z, nt, split, mt, kc0, kc1;
+    int z, nt, split, mt, kc0, kc1;  // mt: the item's first M tile
 };
 
 __device__ __forceinline__ Item decode_item(const Params& p, int item) {
     Item w;
-    w.mt = item % p.m_tiles;
-    int r = item / p.m_tiles;
+    w.mt = (item % p.m_units) * p.MT;
+    int r = item / p.m_units;
     w.split = r % p.splits;
     r /= p.splits;
     w.nt = r % p.n_tiles;
@@ -112,29 +119,67 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// One item's accumulator (TMEM columns 0..BN of `tacc`, this thread's lane
-// quarter already added) to global memory: bf16 rows of `out`, or this
-// split's fp32 rows of the partials.  Runs in the 128 epilogue threads
-// (t = 0..127, row = t in the tile); 32 columns per round through `stg`.
-__device__ __forceinline__ void store_tile(const Params& p, const Item& w, int Z, uint32_t tacc,
-                                           uint8_t* stg, int t, bool fp32) {
-    const int m0 = w.mt * BM, n0 = w.nt * p.BN;
+// TMEM -> registers, 32 lanes x 32 columns, without the wait (issue several,
+// then tmem_wait_ld and tmem_reg_fence on the registers before their use).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Keeps every use of r after the wait: the compiler sees r rewritten here.
+__device__ __forceinline__ void tmem_reg_fence(uint32_t* r, int n) {
+#pragma unroll
+    for (int i = 0; i < n; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// One M tile of an item's accumulator (TMEM columns 0..BN of `tacc`, this
+// thread's lane quarter already added) to global memory: bf16 rows of `out`,
+// or this split's fp32 rows of the partials.  Runs in the 128 epilogue
+// threads (t = 0..127, row = t in the tile); 64 columns per round through
+// `stg`.  When release != 0 the TMEM buffer is handed back (one arrival per
+// warp on that barrier) as soon as the last round's columns are in
+// registers.
+__device__ __forceinline__ void store_tile(const Params& p, const Item& w, int mt, int Z, uint32_t tacc,
+                                           uint8_t* stg, int t, bool fp32, uint32_t release) {
+    const int m0 = mt * BM, n0 = w.nt * p.BN;
     const int n_valid = min(p.BN, p.N - n0);
     const int mv = min(BM, p.M - m0);
     float* stg_f = reinterpret_cast<float*>(stg);
     uint16_t* stg_h = reinterpret_cast<uint16_t*>(stg);
     for (int c0 = 0; c0 < n_valid; c0 += EPI_COLS) {
-        uint32_t r[32];
-        tmem_ld32(tacc + (uint32_t)c0, r);
+        uint32_t r[64];
+        const bool two = c0 + 32 < n_valid;
+        tmem_ld32_nowait(tacc + (uint32_t)c0, r);
+        if (two) tmem_ld32_nowait(tacc + (uint32_t)c0 + 32, r + 32);
+        tmem_wait_ld();
+        tmem_reg_fence(r, 64);
+        if (release != 0 && c0 + EPI_COLS >= n_valid) {
+            tc_fence_before();
+            __syncwarp();
+            if ((t & 31) == 0) mbar_arrive(release);
+        }
+        const int nj = two ? 64 : 32;
         if (fp32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) stg_f[j * BM + t] = __uint_as_float(r[j]);
+            for (int j = 0; j < 64; ++j)
+                if (j < nj) stg_f[j * BM + t] = __uint_as_float(r[j]);
         } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[j]));
-                stg_h[j * BM + t] = *reinterpret_cast<const uint16_t*>(&h);
-            }
+            for (int j = 0; j < 64; ++j)
+                if (j < nj) {
+                    const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(r[j]));
+                    stg_h[j * BM + t] = *reinterpret_cast<const uint16_t*>(&h);
+                }
         }
         epi_sync();
         const int ncols = min(EPI_COLS, n_valid - c0);
@@ -168,8 +213,8 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int Z
 
 // The last CTA to finish a split tile adds every split's fp32 partial in
 // split order and writes the bf16 tile (128 epilogue threads).
-__device__ __forceinline__ void reduce_tile(const Params& p, const Item& w, int Z, int t) {
-    const int m0 = w.mt * BM, n0 = w.nt * p.BN;
+__device__ __forceinline__ void reduce_tile(const Params& p, const Item& w, int mt, int Z, int t) {
+    const int m0 = mt * BM, n0 = w.nt * p.BN;
     const int n_valid = min(p.BN, p.N - n0);
     const int mv = min(BM, p.M - m0);
     const int64_t split_stride = (int64_t)Z * p.N * p.M;
@@ -222,6 +267,9 @@ __device__ __forceinline__ void reduce_tile(const Params& p, const Item& w, int 
     }
 }
 
+// MT (M tiles per item, 1 or 2) is a template parameter: with it known at
+// compile time the product and copy issue loops unroll.
+template <int MT>
 __global__ void __launch_bounds__(THREADS, 1)
 wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
              const __grid_constant__ CUtensorMap tm_x, const Params p) {
@@ -229,20 +277,21 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
     const uint32_t xb = (uint32_t)p.BN * BK * 2;
-    const uint32_t stage_bytes = A_BYTES + xb;  // multiple of 1024 (BN % 16 == 0)
+    const uint32_t a_all = (uint32_t)MT * A_BYTES;
+    const uint32_t stage_bytes = a_all + xb;  // multiple of 1024 (BN % 16 == 0)
     const int S = p.stages;
     uint8_t* stg = smem + S * stage_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(stg + STG_BYTES);
     // bars: [0, S) full, [S, 2S) empty, 2S + b acc_full, 2S + 2 + b acc_empty, 2S + 4 final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
-    int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] skip, [1] this tile's reducer
+    int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] this tile's reducer
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int i0 = (int)((int64_t)p.items * blockIdx.x / gridDim.x);
     const int i1 = (int)((int64_t)p.items * (blockIdx.x + 1) / gridDim.x);
-    const int Z = p.items / (p.n_tiles * p.splits * p.m_tiles);
+    const int Z = p.items / (p.n_tiles * p.splits * p.m_units);
     uint32_t acc_cols = 32;
-    while (acc_cols < (uint32_t)p.BN) acc_cols <<= 1;
+    while (acc_cols < (uint32_t)(MT * p.BN)) acc_cols <<= 1;
     const uint32_t tmem_cols = 2 * acc_cols;
 
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
@@ -258,8 +307,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
             mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
         }
         mbar_init(fin, 1);
-        flag[0] = device_status_raised() ? 1 : 0;  // one decision for the whole CTA
-        flag[1] = 0;
+        flag[0] = 0;
         fence_mbar_init_cluster();
     }
     if (warp == 0 && lane == 0) {
@@ -272,34 +320,40 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const bool skip = flag[0] != 0;
+    // No read of the device status word here (a cold global load on every
+    // CTA's critical path): when another kernel has raised it, the first
+    // wait below that is not met at once gives up and the CTA winds down.
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (!skip && lane == 0) {
+        if (lane == 0) {
             const uint64_t pol_a = p.a_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
             int it = 0;
             bool ok = true;
             for (int item = i0; item < i1 && ok; ++item) {
                 const Item w = decode_item(p, item);
-                const bool second = w.mt >= p.m_split;
-                const CUtensorMap* am = second ? &tm_a2 : &tm_a;
-                const int m0 = (second ? w.mt - p.m_split : w.mt) * BM;
                 const int n0 = w.nt * p.BN;
                 for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
                     const int s = it % S;
                     if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) { ok = false; break; }
                     const uint32_t sa = smem_u32(smem + s * stage_bytes);
-                    const uint32_t sx = sa + A_BYTES;
                     mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
-                    if (p.a_mn) {
-                        tma_load_3d(sa, am, full0 + 8 * s, m0, kc * BK, w.z, pol_a);
-                        tma_load_3d(sa + A_BYTES / 2, am, full0 + 8 * s, m0 + 64, kc * BK, w.z, pol_a);
-                    } else {
-                        tma_load_3d(sa, am, full0 + 8 * s, kc * BK, m0, w.z, pol_a);
+#pragma unroll
+                    for (int j = 0; j < MT; ++j) {
+                        const int mt = w.mt + j;
+                        const bool second = mt >= p.m_split;
+                        const CUtensorMap* am = second ? &tm_a2 : &tm_a;
+                        const int m0 = (second ? mt - p.m_split : mt) * BM;
+                        const uint32_t da = sa + j * A_BYTES;
+                        if (p.a_mn) {
+                            tma_load_3d(da, am, full0 + 8 * s, m0, kc * BK, w.z, pol_a);
+                            tma_load_3d(da + A_BYTES / 2, am, full0 + 8 * s, m0 + 64, kc * BK, w.z, pol_a);
+                        } else {
+                            tma_load_3d(da, am, full0 + 8 * s, kc * BK, m0, w.z, pol_a);
+                        }
                     }
-                    tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? w.z : 0, n0, pol_x);
+                    tma_load_3d(sa + a_all, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? w.z : 0, n0, pol_x);
                 }
             }
             // every issued copy lands before the CTA can exit (on the normal
@@ -309,51 +363,53 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         }
     } else if (warp == 1) {
         // --------------------------------------------------------------- MMA
-        if (!skip) {
-            const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
-            int it = 0, acc = 0;
-            bool ok = true;
-            for (int item = i0; item < i1 && ok; ++item, ++acc) {
-                const Item w = decode_item(p, item);
-                const uint32_t b = acc & 1, use = acc >> 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(acce0 + 8 * b, (use & 1) ^ 1, 0x102));
+        const uint32_t idesc = idesc_bf16(BM, p.BN, p.a_mn != 0, false);
+        int it = 0, acc = 0;
+        bool ok = true;
+        for (int item = i0; item < i1 && ok; ++item, ++acc) {
+            const Item w = decode_item(p, item);
+            const uint32_t b = acc & 1, use = acc >> 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(acce0 + 8 * b, (use & 1) ^ 1, 0x102));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t d = tmem + b * acc_cols;
+            for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
+                const int s = it % S;
+                ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (it / S) & 1, 0x103));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t d = tmem + b * acc_cols;
-                for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
-                    const int s = it % S;
-                    ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (it / S) & 1, 0x103));
-                    if (!ok) break;
-                    tc_fence_after();
-                    if (elect_one_sync()) {
-                        const uint32_t sa = smem_u32(smem + s * stage_bytes);
-                        const uint32_t sx = sa + A_BYTES;
+                if (elect_one_sync()) {
+                    const uint32_t sa = smem_u32(smem + s * stage_bytes);
+                    const uint32_t sx = sa + a_all;
 #pragma unroll
-                        for (int kk = 0; kk < BK / 16; ++kk) {
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t dx = smem_desc(sx + kk * 32, 16, 1024, SWZ_128B);
+#pragma unroll
+                        for (int j = 0; j < MT; ++j) {
                             // A: K-major 128B-swizzled rows of 64 k, +32 B per 16-k step;
                             //    MN-major: two 64-m boxes 8 KB apart, 16 k-rows = 2 KB.
-                            const uint64_t da = p.a_mn ? smem_desc(sa + kk * 2048, 8192, 1024, SWZ_128B)
-                                                       : smem_desc(sa + kk * 32, 16, 1024, SWZ_128B);
-                            const uint64_t dx = smem_desc(sx + kk * 32, 16, 1024, SWZ_128B);
-                            mma_ss(d, da, dx, idesc, (kc > w.kc0 || kk > 0) ? 1u : 0u);
+                            const uint32_t aj = sa + j * A_BYTES;
+                            const uint64_t da = p.a_mn ? smem_desc(aj + kk * 2048, 8192, 1024, SWZ_128B)
+                                                       : smem_desc(aj + kk * 32, 16, 1024, SWZ_128B);
+                            mma_ss(d + j * p.BN, da, dx, idesc, (kc > w.kc0 || kk > 0) ? 1u : 0u);
                         }
-                        tc_commit(empty0 + 8 * s);
                     }
-                    __syncwarp();
+                    tc_commit(empty0 + 8 * s);
                 }
-                if (!ok) break;
-                if (elect_one_sync()) tc_commit(accf0 + 8 * b);
                 __syncwarp();
             }
-            // tracks every product issued, also on the abort path
-            if (elect_one_sync()) tc_commit(fin);
+            if (!ok) break;
+            if (elect_one_sync()) tc_commit(accf0 + 8 * b);
             __syncwarp();
         }
+        // tracks every product issued, also on the abort path
+        if (elect_one_sync()) tc_commit(fin);
+        __syncwarp();
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;
         const int t = q * 32 + lane;  // row of the tile this thread reads from TMEM
-        bool ok = !skip;
+        bool ok = true;
         int acc = 0;
         for (int item = i0; item < i1; ++item, ++acc) {
             const Item w = decode_item(p, item);
@@ -362,32 +418,33 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
             good = epi_sync_and(good);
             ok = good;
             tc_fence_after();
-            if (good)
-                store_tile(p, w, Z, tmem + b * acc_cols + ((uint32_t)(q * 32) << 16), stg, t,
-                           p.mode != OUT_BF16);
-            // the buffer is free for the item after next once this warp's reads are done
-            tc_fence_before();
-            __syncwarp();
-            if (good && lane == 0) mbar_arrive(acce0 + 8 * b);
-            if (p.mode == OUT_REDUCE) {
-                // Every CTA of a split tile arrives on its counter -- also one
-                // that skipped or gave up -- and the last arrival resets it, so
-                // the counters are back at zero for the next call whatever
-                // happened in this one.  Only a last arrival that sees no error
-                // anywhere reduces.
-                __threadfence();
-                epi_sync();
-                if (t == 0) {
-                    const int tile = (w.z * p.n_tiles + w.nt) * p.m_tiles + w.mt;
-                    const int prev = atomicAdd(p.ws_count + tile, 1);
-                    const bool last = prev == p.splits - 1;
-                    if (last) p.ws_count[tile] = 0;
-                    flag[1] = last && good && !device_status_raised() ? 1 : 0;
-                }
-                epi_sync();
-                if (flag[1]) {
+#pragma unroll
+            for (int j = 0; j < MT; ++j) {
+                const int mt = w.mt + j;
+                // the last tile's final TMEM read hands the buffer back
+                if (good)
+                    store_tile(p, w, mt, Z, tmem + b * acc_cols + (uint32_t)(j * p.BN) + ((uint32_t)(q * 32) << 16),
+                               stg, t, p.mode != OUT_BF16, j == MT - 1 ? acce0 + 8 * b : 0u);
+                if (p.mode == OUT_REDUCE) {
+                    // Every CTA of a split tile arrives on its counter -- also
+                    // one that gave up -- and the last arrival resets it, so
+                    // the counters are back at zero for the next call whatever
+                    // happened in this one.  Only a last arrival that sees no
+                    // error anywhere reduces.
                     __threadfence();
-                    reduce_tile(p, w, Z, t);
+                    epi_sync();
+                    if (t == 0) {
+                        const int tile = (w.z * p.n_tiles + w.nt) * p.m_tiles + mt;
+                        const int prev = atomicAdd(p.ws_count + tile, 1);
+                        const bool last = prev == p.splits - 1;
+                        if (last) p.ws_count[tile] = 0;
+                        flag[0] = last && good && !device_status_raised() ? 1 : 0;
+                    }
+                    epi_sync();
+                    if (flag[0]) {
+                        __threadfence();
+                        reduce_tile(p, w, mt, Z, t);
+                    }
                 }
             }
         }
@@ -399,7 +456,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     if (warp == 1) {
-        if (!skip) mbar_wait_teardown(fin, 0, MLA_WAIT_LIMIT_NS);
+        mbar_wait_teardown(fin, 0, MLA_WAIT_LIMIT_NS);
         __syncwarp();
         tmem_dealloc(tmem, tmem_cols);
     }

@@ -90,7 +90,9 @@ bool device_info(DeviceInfo& out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::dec::SMEM_ALLOC) != cudaSuccess)
             return false;
-        if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mla::gemm::SMEM_CAP) != cudaSuccess ||
+            cudaFuncSetAttribute(mla::gemm::wgemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::gemm::SMEM_CAP) != cudaSuccess)
             return false;
         if (cudaFuncSetAttribute(mla::pre::prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -176,7 +178,7 @@ DecodeWs decode_ws_layout(int64_t U, int64_t G, int d_c) {
 // ------------------------------------------------------------- GEMM plan
 
 struct GemmPlan {
-    int BN = 16, n_tiles = 1, m_tiles = 1, splits = 1, chunks = 1, items = 0, grid = 0, stages = 1;
+    int BN = 16, n_tiles = 1, m_tiles = 1, MT = 1, splits = 1, chunks = 1, items = 0, grid = 0, stages = 1;
     int mode = mla::gemm::OUT_BF16;
     size_t smem = 0, ws_part_bytes = 0, ws_count_bytes = 0;
 };
@@ -185,43 +187,64 @@ enum SplitMode : int { kNoSplit = 0, kSplitReduce = 1, kSplitParts = 2 };
 
 // The GEMM's work plan for D [M x N] per head z (M rows that exist, a
 // multiple of 8) with reduction length K.  One CTA per SM walks a
-// contiguous range of items; the K split is chosen by a cost in units of one
-// A chunk (16 KB): the larger of the evenly shared stream (all tiles' chunks
-// over the SMs) and the busiest CTA's chunks at twice the fair per-SM rate,
-// plus the fp32 partials each split writes and the reduction reads.
-GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max_splits = 64) {
+// contiguous range of items.  The M tiles per item (MT) and the K split are
+// chosen by a cost in SM cycles: the largest of the weight stream at the
+// HBM rate, the busiest CTA's chunks (each bound by its TMA rows, about 3.1
+// cycles per 128-byte row, measured, or by its products, about BN / 2
+// cycles per 16-deep step of one M tile), and its epilogue stores (about 20
+// bytes per cycle per SM, measured); plus the last item's stores and, for a
+// split reduced in the kernel, the reducing CTA's reads.  A K split is
+// considered only for few output tiles and a workspace below 256 MB; of two
+// plans within 2 % of each other the one with fewer TMA rows per CTA wins.
+GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max_splits = 64,
+                   bool allow_pairs = true) {
+    const double kRow = 3.1, kHbm = 3150.0, kStore = 20.0, kL2 = 64.0;
     GemmPlan g;
     g.BN = N >= 256 ? 256 : ((N + 15) / 16) * 16;
     g.n_tiles = (N + g.BN - 1) / g.BN;
     g.m_tiles = (M + mla::gemm::BM - 1) / mla::gemm::BM;
     const int kc = K / mla::gemm::BK;
-    const int64_t tiles = (int64_t)Z * g.m_tiles * g.n_tiles;
-    const double epi = g.BN / 32.0;  // an fp32 partial tile, in A chunks
-    double best = 1e300;
-    int best_s = 1;
-    const int s_max = split == kNoSplit ? 1 : std::max(1, std::min(kc, max_splits));
-    for (int s = 1; s <= s_max; ++s) {
-        const int cps = (kc + s - 1) / s;
-        if ((kc + cps - 1) / cps != s) continue;  // the same cut as a smaller s
-        const int64_t items = tiles * s;
-        const int64_t G = std::min<int64_t>(items, sms);
-        const int64_t per = (items + G - 1) / G;
-        double cost = std::max((double)tiles * kc / sms, (double)per * cps / 2.0);
-        if (split == kSplitParts) cost += 0.5 * per * epi;
-        else if (s > 1) cost += 0.5 * per * epi + 0.25 * s * epi;
-        if (cost < best - 1e-9) {
-            best = cost;
-            best_s = s;
+    const double a_bytes = 2.0 * Z * g.m_tiles * mla::gemm::BM * (double)K;
+    double best = 1e300, best_tma = 1e300;
+    int best_s = 1, best_mt = 1;
+    for (int MT = 1; MT <= 2; ++MT) {
+        if (MT == 2 && (!allow_pairs || g.m_tiles % 2 != 0 || g.BN > 128)) continue;
+        const int64_t units = (int64_t)Z * (g.m_tiles / MT) * g.n_tiles;
+        const bool few = split == kSplitParts || units < 2 * (int64_t)sms;
+        const int s_max = split == kNoSplit || !few ? 1 : std::max(1, std::min(kc, max_splits));
+        for (int s = 1; s <= s_max; ++s) {
+            const int cps = (kc + s - 1) / s;
+            if ((kc + cps - 1) / cps != s) continue;  // the same cut as a smaller s
+            const int64_t items = units * s;
+            const int64_t G = std::min<int64_t>(items, sms);
+            const int64_t per = (items + G - 1) / G;
+            if (s > 1 && 4.0 * s * Z * (double)N * M > 256.0 * (1 << 20)) continue;
+            const bool fp32 = split == kSplitParts || s > 1;
+            const double tile_store = (double)mla::gemm::BM * g.BN * (fp32 ? 4 : 2) / kStore;
+            const double tma =
+                (double)per * cps * std::max((MT * mla::gemm::BM + g.BN) * kRow, 2.0 * MT * g.BN);
+            const double stores = (double)per * MT * tile_store;
+            double cost = std::max(std::max(a_bytes / kHbm, tma), stores) + MT * tile_store;
+            if (split == kSplitReduce && s > 1)
+                cost += s * (double)mla::gemm::BM * g.BN * 4 / kL2 + (double)mla::gemm::BM * g.BN * 2 / kStore;
+            if (cost < best * (1 - 0.02) || (cost < best * (1 + 0.02) && tma < best_tma)) {
+                best = std::min(best, cost);
+                best_tma = tma;
+                best_s = s;
+                best_mt = MT;
+            }
         }
     }
+    g.MT = best_mt;
     g.chunks = (kc + best_s - 1) / best_s;
     g.splits = (kc + g.chunks - 1) / g.chunks;
     g.mode = split == kSplitParts ? mla::gemm::OUT_PARTS
                                   : (g.splits > 1 ? mla::gemm::OUT_REDUCE : mla::gemm::OUT_BF16);
-    const int64_t items = tiles * g.splits;
+    const int64_t tiles = (int64_t)Z * g.m_tiles * g.n_tiles;
+    const int64_t items = (int64_t)Z * (g.m_tiles / g.MT) * g.n_tiles * g.splits;
     g.items = items > 0x7FFFFFFF ? 0 : (int)items;  // 0: too large (refused by the caller)
     g.grid = (int)std::min<int64_t>(items, sms);
-    const size_t stage = (size_t)mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
+    const size_t stage = (size_t)g.MT * mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
     const size_t fixed = 1024 + mla::gemm::STG_BYTES + 256;
     g.stages = (int)std::min<size_t>(mla::gemm::MAX_STAGES, (mla::gemm::SMEM_CAP - fixed) / stage);
     g.smem = fixed + (size_t)g.stages * stage;
@@ -244,6 +267,8 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
     p.N = N;
     p.K = K;
     p.m_tiles = g.m_tiles;
+    p.MT = g.MT;
+    p.m_units = g.m_tiles / g.MT;
     p.m_split = m_split;
     p.BN = g.BN;
     p.n_tiles = g.n_tiles;
@@ -262,7 +287,10 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
     p.ws_part = ws_part;
     p.ws_count = ws_count;
     (void)Z;
-    mla::gemm::wgemm_kernel<<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
+    if (g.MT == 2)
+        mla::gemm::wgemm_kernel<2><<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
+    else
+        mla::gemm::wgemm_kernel<1><<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
     return launch_status();
 }
 
@@ -608,7 +636,8 @@ bool rope_freqs(uint64_t (&f)[mla::pro::MAX_PAIRS], int d_r, double base) {
 // plan (and so the workspace) depends on d_r only through the number of M
 // tiles, which is d_c / 128 + 1 for every d_r <= 128.
 GemmPlan cache_append_plan(int N, int d, int d_c, int d_r, int sms) {
-    return gemm_plan(d_c + d_r, N, d, 1, sms, kSplitParts);
+    // one A map per item: the pair of M tiles would straddle W^DKV and W^KR
+    return gemm_plan(d_c + d_r, N, d, 1, sms, kSplitParts, 64, false);
 }
 
 size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype) {
