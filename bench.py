@@ -495,13 +495,46 @@ def time_alone(fn, s, flush, steps: int, warmup: int) -> float:
     return statistics.median(times)
 
 
+def time_stream(fns, s, steps: int, warmup: int) -> float:
+    """Per-call device time (us) of calls streamed back to back, as in a
+    decode step: the calls fns, each over its own copy of the inputs (the
+    copies together larger than L2, so that no call finds its weights left
+    in L2 by the one before), are captured in order in one CUDA graph; the
+    graph is replayed between CUDA events and the median replay time is
+    divided by the number of calls.  Unlike time_alone this leaves out the
+    launch of a lone graph, which a step of many kernels pays once."""
+    with torch.cuda.stream(s):
+        for _ in range(warmup):
+            for f in fns:
+                f()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for f in fns:
+            f()
+    times = []
+    with torch.cuda.stream(s):
+        graph.replay()
+        for _ in range(steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            graph.replay()
+            b.record(s)
+            b.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(times) / len(fns)
+
+
 def run_projections(args, local):
     """The query absorption (q_lat = W^UK^T q_nope) and the output projection
     (out = W^O concat_i W^UV_i o_i) at the two-token workload's sizes (64
-    query rows x 128 heads, d_h 128, d_c 512, d 7168), each timed alone: one
-    call captured in a CUDA graph, CUDA events around each replay, L2 flushed
-    (a 256 MB write) before each, median over the timed replays.  Both are bound by their weight bytes
-    (16.8 MB W^UK; 16.8 MB W^UV + 235 MB W^O) against the measured HBM rate."""
+    query rows x 128 heads, d_h 128, d_c 512, d 7168).  Each is timed two
+    ways: streamed back to back over rotating copies of its inputs larger
+    than L2 together (time_stream: "us", the figure the roofline fraction
+    uses), and alone (time_alone: one call in a CUDA graph, L2 flushed by a
+    256 MB write before each replay: "us_alone", which adds the launch of a
+    lone graph).  Both are bound by their weight bytes (16.8 MB W^UK;
+    16.8 MB W^UV + 235 MB W^O) against the measured HBM rate."""
     from mla_latent_kv_71_b300 import mla
     dev = torch.device("cuda", local)
     spec = workloads.WORKLOADS["mtp_b32_t2_l8192"]
@@ -523,21 +556,31 @@ def run_projections(args, local):
     def timed(fn):
         return time_alone(fn, s, flush, args.steps, args.warmup)
 
+    # rotating copies: 8 x 27 MB for the query absorption, 2 x 265 MB for
+    # the output projection
+    absorb_sets = [(qn.clone(), w_uk.clone(), torch.empty_like(q_lat)) for _ in range(8)]
+    out_sets = [(o.clone(), w_uv.clone(), w_o.clone(), torch.empty_like(v_tmp), torch.empty_like(out),
+                 torch.zeros_like(ws)) for _ in range(2)]
     pk, pk_kind = peaks()
-    res = {"metric": "MLA decode projections alone, weight GB/s vs measured HBM", "rows": rows, "H": H,
+    res = {"metric": "MLA decode projections, weight GB/s vs measured HBM", "rows": rows, "H": H,
            "d_h": d_h, "d_c": d_c, "d": d, "dtype": "bf16", "data": "synthetic",
-           "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
+           "timing": (f"us: median of {args.steps} replays of a graph of calls back to back over "
+                      f"rotating input copies larger than L2, per call; us_alone: median of "
+                      f"{args.steps} graph replays of one call, L2 flushed before each"),
            "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
-    for name, fn, wbytes, other, flops in (
-            ("absorb_q", lambda: mla.absorb_q(qn, w_uk, q_lat, stream=s), w_uk.numel() * 2,
-             (qn.numel() + q_lat.numel()) * 2, 2 * rows * H * d_h * d_c),
+    for name, fn, fns, wbytes, other, flops in (
+            ("absorb_q", lambda: mla.absorb_q(qn, w_uk, q_lat, stream=s),
+             [(lambda a=a: mla.absorb_q(a[0], a[1], a[2], stream=s)) for a in absorb_sets],
+             w_uk.numel() * 2, (qn.numel() + q_lat.numel()) * 2, 2 * rows * H * d_h * d_c),
             ("out_proj", lambda: mla.out_proj(o, w_uv, w_o, v_tmp, out, ws, stream=s),
+             [(lambda a=a: mla.out_proj(*a, stream=s)) for a in out_sets],
              (w_uv.numel() + w_o.numel()) * 2, (o.numel() + 2 * v_tmp.numel() + out.numel()) * 2,
              2 * rows * H * d_h * d_c + 2 * rows * d * H * d_h)):
-        us = timed(fn)
+        us = time_stream(fns, s, args.steps, args.warmup)
+        us_alone = timed(fn)
         gbs = (wbytes + other) / (us * 1e-6) / 1e9
-        res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
-                     "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12}
+        res[name] = {"us": us, "us_alone": us_alone, "weight_bytes": wbytes, "bytes": wbytes + other,
+                     "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12}
     code, detail = mla.get_device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} detail {detail:#x}")
@@ -596,7 +639,8 @@ def run_prefill(args, local):
 
 
 def run_prologue(args, local):
-    """The steps before the decode, each timed alone like --projections: the
+    """The steps before the decode, each timed like --projections (streamed
+    over rotating input copies, and alone): the
     cache write of one new token per sequence of the headline batch (64
     tokens at position 4096: c = W^DKV h and k^R = RoPE(W^KR h) from d = 7168
     into the paged pool) and the query of those tokens (W^Q c^Q from the
@@ -631,26 +675,37 @@ def run_prologue(args, local):
     def timed(fn):
         return time_alone(fn, s, flush, args.steps, args.warmup)
 
+    # rotating copies: 16 x 8.3 MB of W^DKV, W^KR; 3 x 75.5 MB of W^Q
+    kv_sets = [(w_dkv.clone(), w_kr.clone(), torch.zeros_like(ws_kv)) for _ in range(16)]
+    q_sets = [(w_q.clone(), torch.zeros_like(ws_q)) for _ in range(3)]
     pk, pk_kind = peaks()
-    res = {"metric": "MLA decode prologue alone, GB/s vs measured HBM", "tokens": B, "position": pos,
+    res = {"metric": "MLA decode prologue, GB/s vs measured HBM", "tokens": B, "position": pos,
            "d": d, "d_c": d_c, "d_r": d_r, "H": H, "d_h": d_h, "d_q": d_q, "dtype": "bf16",
-           "data": "synthetic", "timing": f"median of {args.steps} graph replays of one call, L2 flushed before each",
+           "data": "synthetic",
+           "timing": (f"us: median of {args.steps} replays of a graph of calls back to back over "
+                      f"rotating weight copies larger than L2, per call; us_alone: median of "
+                      f"{args.steps} graph replays of one call, L2 flushed before each"),
            "peak_hbm_gbs": pk["hbm_gbs"], "peak_kind": pk_kind}
-    for name, fn, wbytes, other, flops, launches in (
+    for name, fn, fns, wbytes, other, flops, launches in (
             ("cache_append",
              lambda: mla.cache_append(h, w_dkv, w_kr, seq_ids, positions, table, pool, workspace=ws_kv,
                                       stream=s),
+             [(lambda a=a: mla.cache_append(h, a[0], a[1], seq_ids, positions, table, pool, workspace=a[2],
+                                             stream=s)) for a in kv_sets],
              (w_dkv.numel() + w_kr.numel()) * 2, h.numel() * 2 + B * (d_c + d_r) * 2,
              2 * B * (d_c + d_r) * d, 2),
             ("project_q",
              lambda: mla.project_q(c_q, w_q, positions, H, d_h, d_r, q_nope, q_pe, workspace=ws_q,
                                    stream=s),
+             [(lambda a=a: mla.project_q(c_q, a[0], positions, H, d_h, d_r, q_nope, q_pe, workspace=a[1],
+                                          stream=s)) for a in q_sets],
              w_q.numel() * 2, c_q.numel() * 2 + (q_nope.numel() + q_pe.numel()) * 2,
              2 * B * H * (d_h + d_r) * d_q, 2)):
-        us = timed(fn)
+        us = time_stream(fns, s, args.steps, args.warmup)
+        us_alone = timed(fn)
         gbs = (wbytes + other) / (us * 1e-6) / 1e9
-        res[name] = {"us": us, "weight_bytes": wbytes, "bytes": wbytes + other, "gbs": gbs,
-                     "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12,
+        res[name] = {"us": us, "us_alone": us_alone, "weight_bytes": wbytes, "bytes": wbytes + other,
+                     "gbs": gbs, "frac_hbm": gbs / pk["hbm_gbs"], "tflops": flops / (us * 1e-6) / 1e12,
                      "launches_per_call": launches}
     code, detail = mla.get_device_status()
     if code != 0:

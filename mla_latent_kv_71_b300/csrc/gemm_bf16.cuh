@@ -39,6 +39,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "pdl.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 
@@ -320,6 +321,12 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // The kernel may have been launched before the one ahead of it on the
+    // stream finished (pdl.cuh): the set-up above touched no global memory;
+    // from here on every thread may.  The next kernel may launch now: it
+    // waits the same way before it reads what this one writes.
+    grid_dep_wait();
+    if (threadIdx.x == 0) grid_dep_launch();
     // No read of the device status word here (a cold global load on every
     // CTA's critical path): when another kernel has raised it, the first
     // wait below that is not met at once gives up and the CTA winds down.
@@ -329,32 +336,48 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         if (lane == 0) {
             const uint64_t pol_a = p.a_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
-            int it = 0;
-            bool ok = true;
-            for (int item = i0; item < i1 && ok; ++item) {
-                const Item w = decode_item(p, item);
-                const int n0 = w.nt * p.BN;
-                for (int kc = w.kc0; kc < w.kc1; ++kc, ++it) {
-                    const int s = it % S;
-                    if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) { ok = false; break; }
-                    const uint32_t sa = smem_u32(smem + s * stage_bytes);
-                    mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+            // the copies of one chunk into stage s: A (MT tiles), then X
+            auto load_a = [&](const Item& w, int kc, int s) {
+                const uint32_t sa = smem_u32(smem + s * stage_bytes);
 #pragma unroll
-                    for (int j = 0; j < MT; ++j) {
-                        const int mt = w.mt + j;
-                        const bool second = mt >= p.m_split;
-                        const CUtensorMap* am = second ? &tm_a2 : &tm_a;
-                        const int m0 = (second ? mt - p.m_split : mt) * BM;
-                        const uint32_t da = sa + j * A_BYTES;
-                        if (p.a_mn) {
-                            tma_load_3d(da, am, full0 + 8 * s, m0, kc * BK, w.z, pol_a);
-                            tma_load_3d(da + A_BYTES / 2, am, full0 + 8 * s, m0 + 64, kc * BK, w.z, pol_a);
-                        } else {
-                            tma_load_3d(da, am, full0 + 8 * s, kc * BK, m0, w.z, pol_a);
-                        }
+                for (int j = 0; j < MT; ++j) {
+                    const int mt = w.mt + j;
+                    const bool second = mt >= p.m_split;
+                    const CUtensorMap* am = second ? &tm_a2 : &tm_a;
+                    const int m0 = (second ? mt - p.m_split : mt) * BM;
+                    const uint32_t da = sa + j * A_BYTES;
+                    if (p.a_mn) {
+                        tma_load_3d(da, am, full0 + 8 * s, m0, kc * BK, w.z, pol_a);
+                        tma_load_3d(da + A_BYTES / 2, am, full0 + 8 * s, m0 + 64, kc * BK, w.z, pol_a);
+                    } else {
+                        tma_load_3d(da, am, full0 + 8 * s, kc * BK, m0, w.z, pol_a);
                     }
-                    tma_load_3d(sa + a_all, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? w.z : 0, n0, pol_x);
                 }
+            };
+            auto load_x = [&](const Item& w, int kc, int s) {
+                const uint32_t sx = smem_u32(smem + s * stage_bytes) + a_all;
+                tma_load_3d(sx, &tm_x, full0 + 8 * s, kc * BK, p.x_batched ? w.z : 0, w.nt * p.BN, pol_x);
+            };
+            // The chunks of the CTA's items in order, as (item, kc).
+            int item = i0, kc = 0;
+            Item w{};
+            if (item < i1) {
+                w = decode_item(p, item);
+                kc = w.kc0;
+            }
+            auto next = [&]() {
+                if (++kc >= w.kc1 && ++item < i1) {
+                    w = decode_item(p, item);
+                    kc = w.kc0;
+                }
+            };
+            int it = 0;
+            for (; item < i1; ++it, next()) {
+                const int s = it % S;
+                if (!mbar_wait(empty0 + 8 * s, ((it / S) & 1) ^ 1, 0x101)) break;
+                mbar_arrive_expect_tx(full0 + 8 * s, stage_bytes);
+                load_a(w, kc, s);
+                load_x(w, kc, s);
             }
             // every issued copy lands before the CTA can exit (on the normal
             // path these phases have completed; after an abort they may not)

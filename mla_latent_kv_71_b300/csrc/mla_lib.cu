@@ -10,6 +10,7 @@
 #include <cstring>
 #include <atomic>
 #include <mutex>
+#include <utility>
 #include <vector>
 
 #include "../../include/mla.h"
@@ -127,6 +128,25 @@ bool device_info(DeviceInfo& out) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Status of the launch(es) just made; counts `n` launched kernels.
+// Launch with programmatic stream serialization (pdl.cuh): the kernel may
+// start its set-up while the one before it on the stream finishes.
+template <typename... KArgs, typename... Args>
+mla_status_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                        Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...) == cudaSuccess ? MLA_OK
+                                                                                          : MLA_ERR_CUDA;
+}
+
 mla_status_t launch_status(int n = 1) {
     if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
     g_launches += n;
@@ -287,10 +307,10 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
     p.ws_part = ws_part;
     p.ws_count = ws_count;
     (void)Z;
-    if (g.MT == 2)
-        mla::gemm::wgemm_kernel<2><<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
-    else
-        mla::gemm::wgemm_kernel<1><<<(unsigned)g.grid, mla::gemm::THREADS, g.smem, st>>>(ta, ta2, tx, p);
+    const mla_status_t s = launch_pdl(g.MT == 2 ? mla::gemm::wgemm_kernel<2> : mla::gemm::wgemm_kernel<1>,
+                                      dim3((unsigned)g.grid), dim3(mla::gemm::THREADS), g.smem, st, ta, ta2,
+                                      tx, p);
+    if (s != MLA_OK) return s;
     return launch_status();
 }
 
@@ -712,7 +732,8 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
     p.splits = g.splits;
     const unsigned threads = (unsigned)(((d_c + d_r) / 2 + 31) / 32 * 32);
     if (threads > 1024) return MLA_ERR_UNSUPPORTED;
-    mla::pro::kv_finish_bf16_kernel<<<(unsigned)N, threads, 0, st>>>(p);
+    s = launch_pdl(mla::pro::kv_finish_bf16_kernel, dim3((unsigned)N), dim3(threads), 0, st, p);
+    if (s != MLA_OK) return s;
     return launch_status();
 }
 
@@ -778,7 +799,8 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
     p.parts = ws_parts(g, workspace);
     p.splits = g.splits;
     const dim3 grid((unsigned)N, (unsigned)((H + mla::pro::Q_HEADS - 1) / mla::pro::Q_HEADS));
-    mla::pro::q_finish_bf16_kernel<<<grid, (unsigned)threads, 0, st>>>(p);
+    s = launch_pdl(mla::pro::q_finish_bf16_kernel, grid, dim3((unsigned)threads), 0, st, p);
+    if (s != MLA_OK) return s;
     return launch_status();
 }
 

@@ -34,6 +34,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "pdl.cuh"
 #include "status.cuh"
 
 namespace mla {
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(THREADS) kv_rows_fp32_kernel(const KvParams p)
 // it, so that the block writes the whole pool row in one pass.
 __global__ void kv_finish_bf16_kernel(const KvParams p) {
     __shared__ __nv_bfloat16* row;
+    grid_dep_wait();  // the GEMM's partials (launched as its dependent, pdl.cuh)
     if (threadIdx.x == 0) row = device_status_raised() ? nullptr : kv_row<__nv_bfloat16>(p, blockIdx.x);
     __syncthreads();
     if (row == nullptr) return;
@@ -282,6 +284,7 @@ __global__ void __launch_bounds__(THREADS) q_rows_fp32_kernel(const QParams p) {
 // bf16 and stores it to q_nope or q_pe.
 __global__ void q_finish_bf16_kernel(const QParams p) {
     __shared__ int stop;
+    grid_dep_wait();  // the GEMM's partials (launched as its dependent, pdl.cuh)
     if (threadIdx.x == 0) stop = device_status_raised() ? 1 : 0;
     __syncthreads();
     if (stop) return;
