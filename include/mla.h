@@ -162,7 +162,7 @@ mla_status_t mla_decode_attn_partial(const void* q_lat, const void* q_pe, const 
 /*
  * mla_decode_plan -- how mla_decode_attn (bf16) divides a batch over the GPU,
  * computed on the host from the same arithmetic the kernel uses.
- * The pages of all units u = (b*T + t)*ceil(H/128) + head_group are laid end
+ * The pages of all units u = (t*ceil(H/128) + head_group)*B + b are laid end
  * to end on a line where each non-empty unit after the first is preceded by
  * 3 virtual pages when the line holds at least 8 pages per cluster (starting
  * a unit piece costs a cluster about that much), and the line is cut into

@@ -184,6 +184,20 @@ __host__ __device__ __forceinline__ int virtual_total(int total, int units, int 
     return units > 0 ? total + C * (units - 1) : 0;
 }
 
+// Line order of the units: u = (t * HG + hg) * B + b.  Each query token
+// (and head group) of the batch is a stretch of the line of about the same
+// length, so the clusters at the same offset of each stretch read the same
+// pages at about the same time, and the later read of a page finds it in L2
+// (with T query tokens a page is needed T times; one after another within a
+// cluster's range, the reads would be some tens of microseconds apart, and
+// most would miss).
+__host__ __device__ __forceinline__ void unit_index(int u, int B, int HG, int& b, int& t, int& hg) {
+    b = u % B;
+    const int r = u / B;
+    hg = r % HG;
+    t = r / HG;
+}
+
 // Visible positions and pages of unit u.
 struct Unit {
     int b, t, hg;
@@ -194,10 +208,7 @@ struct Unit {
 
 __host__ __device__ __forceinline__ Unit unit_of(const PlanView& v, int u) {
     Unit r;
-    const int bt = u / v.HG;
-    r.hg = u % v.HG;
-    r.b = bt / v.T;
-    r.t = bt % v.T;
+    unit_index(u, v.B, v.HG, r.b, r.t, r.hg);
     int len = v.seq_lens[r.b];
     const int cap = v.max_pages * PAGE;
     r.bad_len = len < 0 || len > cap;
@@ -561,8 +572,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         Walker w = walk;
         Segment sg;
         while (w.next(pv, sg)) {
-            const int bt = sg.u / p.HG;  // unit u = (b * T + t) * HG + hg
-            const int head0 = (sg.u - bt * p.HG) * HEADS;
+            int ub, ut, uh;
+            unit_index(sg.u, p.B, p.HG, ub, ut, uh);
+            const int bt = ub * p.T + ut;  // row of q, o
+            const int head0 = uh * HEADS;
             const int rows = min(HEADS, p.H - head0);
             const int64_t qrow0 = (int64_t)bt * p.H + head0;
             bulk_prefetch_l2(p.q_lat + qrow0 * DC, (uint32_t)rows * DC * 2u);
@@ -605,7 +618,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 ok = mbar_wait(EMPTY(s), (uint32_t)((it / NSTAGE) & 1) ^ 1u, 0x201);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const int b_seq = sg.u / (p.HG * p.T);  // unit u = (b * T + t) * HG + hg
+                const int b_seq = sg.u % p.B;  // unit u = (t * HG + hg) * B + b
                 int64_t pg = p.page_table[(int64_t)b_seq * p.max_pages + lp];
                 if (pg < 0 || pg >= p.num_pages) {
                     raise_device_status(MLA_DEV_BOUNDS, 0x20);
@@ -785,8 +798,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 // score product of the tile before has completed.
                 if (i >= 1 && !__all_sync(0xffffffffu, mbar_wait(S_FULL((i - 1) % NS), s_par(i - 1), 0x501)))
                     return false;
-                const int bt = t.sg.u / p.HG;  // unit u = (b * T + t) * HG + hg
-                const int head = (t.sg.u - bt * p.HG) * HEADS + h;
+                int ub, ut, uh;
+                unit_index(t.sg.u, p.B, p.HG, ub, ut, uh);
+                const int bt = ub * p.T + ut;  // row of q, o
+                const int head = uh * HEADS + h;
                 const bool live = head < p.H;
                 const int64_t qrow = (int64_t)bt * p.H + head;
                 const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat + qrow * DC + rank * HALF_C);
@@ -996,8 +1011,10 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 const float f_oth = c.first ? 0.f : ex2(m_oth - m_used);
                 const float l = l_part + l_oth * f_oth;     // for lse
                 const float lr = lr_part + lr_oth * f_oth;  // for o
-                const int bt = c.u / p.HG;  // unit u = (b * T + t) * HG + hg
-                const int head0 = (c.u - bt * p.HG) * HEADS + q4 * 32;  // head of this warp's row 0
+                int ub, ut, uh;
+                unit_index(c.u, p.B, p.HG, ub, ut, uh);
+                const int bt = ub * p.T + ut;  // row of q, o
+                const int head0 = uh * HEADS + q4 * 32;  // head of this warp's row 0
                 const int64_t qrow0 = (int64_t)bt * p.H + head0;
                 const float inv_l = 1.f / lr;
                 // Rows go out through this tile's X buffer (the 4 KB this warp
@@ -1153,8 +1170,10 @@ decode_combine_kernel(const Params p) {
     const int row = blockIdx.x * COMBINE_ROWS + warp;  // u * HEADS + h
     const int u = row / HEADS, h = row % HEADS;
     if (u >= p.B * p.T * p.HG) return;
-    const int bt = u / p.HG;  // unit u = (b * T + t) * HG + hg
-    const int head = (u - bt * p.HG) * HEADS + h;
+    int ub, ut, uh;
+    unit_index(u, p.B, p.HG, ub, ut, uh);
+    const int bt = ub * p.T + ut;  // row of q, o
+    const int head = uh * HEADS + h;
     if (head >= p.H) return;
     const PlanView pv{p.seq_lens, p.B, p.T, p.HG, p.max_pages, p.causal};
     const int2 gg = p.ws_unit[u];         // issued together with the length read below

@@ -20,11 +20,13 @@ def check_plan(lens, T, H, max_pages, causal, clusters):
     pieces = mla.decode_plan(lens, T, H, max_pages, causal, clusters)
     HG = (H + 127) // 128
     U = len(lens) * T * HG
+    # units lie on the line in the order u = (t * HG + hg) * B + b
     pages = []
-    for b, n in enumerate(lens):
-        for t in range(T):
-            v = max(0, n - (T - 1 - t)) if causal else n
-            pages += [math.ceil(v / 64)] * HG
+    for t in range(T):
+        for hg in range(HG):
+            for n in lens:
+                v = max(0, n - (T - 1 - t)) if causal else n
+                pages.append(math.ceil(v / 64))
     total = sum(pages)
     G = min(clusters, total)
     seen = {}
