@@ -46,6 +46,27 @@ constexpr int ROWS = 8;       // weight rows (outputs) per block (fp32 kernels)
 constexpr int MAX_PAIRS = 64; // d_r <= 128
 constexpr int Q_HEADS = 4;    // heads per block of the bf16 query finish
 
+// sum over the K splits, in split order, of the fp32 pair at src in each
+// split's partials (split_stride floats apart).  The loads of eight splits
+// are issued together: a split count in the tens would otherwise make this
+// a chain of dependent L2 round trips.
+__device__ __forceinline__ float2 sum_splits(const float* src, int64_t split_stride, int splits) {
+    float a = 0.f, b = 0.f;
+    for (int s0 = 0; s0 < splits; s0 += 8) {
+        float2 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[k] = s0 + k < splits ? __ldcg(reinterpret_cast<const float2*>(src + (s0 + k) * split_stride))
+                                   : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            a += v[k].x;
+            b += v[k].y;
+        }
+    }
+    return make_float2(a, b);
+}
+
 // sin and cos of the angle pos * f, f given as the 0.64 fixed-point
 // fraction of a turn described above.
 __device__ __forceinline__ void rope_sincos(int64_t pos, uint64_t f, float& sn, float& cs) {
@@ -210,14 +231,8 @@ __global__ void kv_finish_bf16_kernel(const KvParams p) {
     const int e = 2 * (int)threadIdx.x;
     if (e >= E) return;
     const int n = blockIdx.x;
-    const int64_t split_stride = (int64_t)p.N * E;
-    const float* src = p.parts + (int64_t)n * E + e;
-    float a = 0.f, b = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + s * split_stride));
-        a += v.x;
-        b += v.y;
-    }
+    const float2 ab = sum_splits(p.parts + (int64_t)n * E + e, (int64_t)p.N * E, p.splits);
+    float a = ab.x, b = ab.y;
     if (e >= p.d_c) {
         float sn, cs;
         rope_sincos(p.positions[n], p.freq[(e - p.d_c) / 2], sn, cs);
@@ -294,14 +309,8 @@ __global__ void q_finish_bf16_kernel(const QParams p) {
     if (i >= p.H) return;
     const int n = blockIdx.x;
     const int M = p.H * qw;
-    const int64_t split_stride = (int64_t)p.N * M;
-    const float* src = p.parts + (int64_t)n * M + (int64_t)i * qw + f;
-    float a = 0.f, b = 0.f;
-    for (int s = 0; s < p.splits; ++s) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + s * split_stride));
-        a += v.x;
-        b += v.y;
-    }
+    const float2 ab = sum_splits(p.parts + (int64_t)n * M + (int64_t)i * qw + f, (int64_t)p.N * M, p.splits);
+    float a = ab.x, b = ab.y;
     const int64_t ni = (int64_t)n * p.H + i;
     if (f < p.d_h) {
         *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.q_nope) + ni * p.d_h + f) =
