@@ -168,7 +168,11 @@ mla_status_t mla_decode_attn_partial(const void* q_lat, const void* q_pe, const 
  * a unit piece costs a cluster about that much), and the line is cut into
  * min(clusters, total pages) equal contiguous ranges, one per 2-CTA cluster;
  * a unit cut by a range boundary is computed in pieces whose partial results
- * are merged by log-sum-exp.
+ * are merged by log-sum-exp.  When every non-empty unit has the same number
+ * of pages n, there are no more units than clusters, and n exceeds the
+ * largest range of the cut by at most 16 pages, one cluster per unit is
+ * launched instead (no unit is cut, no merge step runs); mla_decode_attn
+ * does this only when given seq_lens_host.
  *   seq_lens_host [B] int32 (host), clusters: co-resident clusters (0 = the
  *   current device's value).
  *   out: up to `cap` rows of 7 int64: (cluster, unit, first page, end page

@@ -277,12 +277,17 @@ def test_bf16_out_proj(rows, H, d):
 @pytest.mark.parametrize("name", ["decode_b64_h128_l4096", "ragged_b128_l16k", "long_b4_l128k"])
 def test_full_size_workloads_every_row(name):
     """The GPU over the whole workload, in the launch configuration the bench
-    times; the oracle on every (sequence, token, head) row."""
+    times (lengths also on the host: at the headline batch that is one
+    cluster per sequence, no unit cut), and without host lengths (all
+    clusters, units cut and merged); the oracle on every (sequence, token,
+    head) row of both."""
     case = workloads.make_workload(name, device="cuda")
-    o, lse = _run_decode(case)
-    assert torch.isfinite(lse).all() and torch.isfinite(o.float()).all()
     o_ref, lse_ref = _oracle_decode(case)
-    _check_o_lse(o, lse, o_ref, lse_ref, name, case)
+    for host in (True, False):
+        o, lse = _run_decode(case, seq_lens_host=case.seq_lens.cpu() if host else None)
+        assert torch.isfinite(lse).all() and torch.isfinite(o.float()).all()
+        _check_o_lse(o, lse, o_ref, lse_ref, f"{name} ({'host lengths' if host else 'device lengths'})",
+                     case)
 
 
 @pytest.mark.parametrize("name", ["mtp_b32_t2_l8192", "smallhead_b64_h16_l32k"])

@@ -16,17 +16,37 @@ import pytest
 from mla_latent_kv_71_b300 import mla, workloads
 
 
-def check_plan(lens, T, H, max_pages, causal, clusters):
-    pieces = mla.decode_plan(lens, T, H, max_pages, causal, clusters)
-    HG = (H + 127) // 128
-    U = len(lens) * T * HG
+def unit_pages(lens, T, H, causal):
     # units lie on the line in the order u = (t * HG + hg) * B + b
+    HG = (H + 127) // 128
     pages = []
     for t in range(T):
         for hg in range(HG):
             for n in lens:
                 v = max(0, n - (T - 1 - t)) if causal else n
                 pages.append(math.ceil(v / 64))
+    return pages
+
+
+def launched_clusters(pages, clusters):
+    """One cluster per unit when all non-empty units have the same pages n,
+    there are at most `clusters` of them, and n exceeds the largest range of
+    the cut over all clusters by at most 16 pages; else `clusters`."""
+    ne = [n for n in pages if n]
+    if not ne or len(set(ne)) != 1 or len(ne) > clusters:
+        return clusters
+    total = sum(ne)
+    C = 3 if total >= 8 * clusters else 0
+    V = total + C * (len(ne) - 1)
+    return len(ne) if ne[0] - math.ceil(V / clusters) <= 16 else clusters
+
+
+def check_plan(lens, T, H, max_pages, causal, clusters):
+    pieces = mla.decode_plan(lens, T, H, max_pages, causal, clusters)
+    HG = (H + 127) // 128
+    U = len(lens) * T * HG
+    pages = unit_pages(lens, T, H, causal)
+    clusters = launched_clusters(pages, clusters)
     total = sum(pages)
     G = min(clusters, total)
     seen = {}
@@ -111,3 +131,16 @@ def test_random_plans():
 def test_uniform_batch_is_not_split_when_clusters_divide_it():
     pieces = check_plan([4096] * 64, 1, 128, 64, False, 64)
     assert all(p["slot"] == -1 for p in pieces)
+
+
+def test_uniform_headline_batch_takes_one_cluster_per_sequence():
+    """64 sequences of 4096 on 74 clusters: 64 clusters, no unit cut (the
+    step without the merge kernel measured faster); 64 x 32768 with 16
+    heads keeps all 74 clusters and cuts units (512 pages per cluster would
+    be 69 more than the cut's largest range)."""
+    pieces = check_plan([4096] * 64, 1, 128, 64, False, 74)
+    assert len({p["cluster"] for p in pieces}) == 64
+    assert all(p["slot"] == -1 for p in pieces)
+    pieces = check_plan([32768] * 64, 1, 16, 512, False, 74)
+    assert len({p["cluster"] for p in pieces}) == 74
+    assert any(p["slot"] != -1 for p in pieces)
