@@ -472,6 +472,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         tma_prefetch_desc(&tm_r);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), TM_COLS);
+    // This CTA's barriers are initialised (thread 0, fenced above): its half
+    // of the cluster barrier is passed now, and the wait for the peer's half
+    // comes after the plan, before any remote access, so the round trip
+    // overlaps the plan instead of following it.
+    cluster_arrive_relaxed();
 
     // ---------------------------------------------------------------- plan
     // Every CTA derives the same cut of the page line from seq_lens.
@@ -598,7 +603,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     tc_fence_after();
     // The peer's barriers are initialised before any remote access (their
     // arming needs no order: transaction bytes may land before it).
-    cluster_sync_relaxed();
+    cluster_wait();
     const uint32_t tmem = *tmem_slot;
     const int64_t n_tiles = misc[6];
 
@@ -806,25 +811,28 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                 const int64_t qrow = (int64_t)bt * p.H + head;
                 const uint4* ql = reinterpret_cast<const uint4*>(p.q_lat + qrow * DC + rank * HALF_C);
                 const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + qrow * DR + rank * HALF_R);
-                {   // RoPE columns into shared memory: row h, 16-byte chunk c
-                    // at chunk c ^ ((h / 2) % 4) of its 64 bytes (64-byte swizzle)
-                    uint4 v[4];
+                // The RoPE columns and the first 128 latent columns are
+                // loaded together (one round trip instead of two), then the
+                // other 128.
+                uint4 v[4];
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) v[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
-                    uint8_t* row = smem + OFF_QPE + h * 64;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + 16 * (c ^ ((h >> 1) & 3))) = v[c];
-                }
+                for (int c = 0; c < 4; ++c) v[c] = live ? __ldg(qp + c) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {  // latent columns into TMEM, 128 at a time
                     uint32_t r[64];
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        const uint4 x = live ? __ldg(ql + 16 * half + v) : make_uint4(0u, 0u, 0u, 0u);
-                        r[4 * v] = x.x;
-                        r[4 * v + 1] = x.y;
-                        r[4 * v + 2] = x.z;
-                        r[4 * v + 3] = x.w;
+                    for (int k = 0; k < 16; ++k) {
+                        const uint4 x = live ? __ldg(ql + 16 * half + k) : make_uint4(0u, 0u, 0u, 0u);
+                        r[4 * k] = x.x;
+                        r[4 * k + 1] = x.y;
+                        r[4 * k + 2] = x.z;
+                        r[4 * k + 3] = x.w;
+                    }
+                    if (half == 0) {  // RoPE columns into shared memory: row h, 16-byte chunk c
+                                      // at chunk c ^ ((h / 2) % 4) of its 64 bytes (64-byte swizzle)
+                        uint8_t* row = smem + OFF_QPE + h * 64;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(row + 16 * (c ^ ((h >> 1) & 3))) = v[c];
                     }
                     tmem_st32(trow + TM_Q + 64 * half, *reinterpret_cast<const uint32_t(*)[32]>(r));
                     tmem_st32(trow + TM_Q + 64 * half + 32, *reinterpret_cast<const uint32_t(*)[32]>(r + 32));

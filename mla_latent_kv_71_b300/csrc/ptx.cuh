@@ -223,6 +223,12 @@ __device__ __forceinline__ uint32_t num_clusters_x() {
 // Cluster barrier whose arrive orders nothing: for the start of a kernel,
 // after fence.mbarrier_init has published this CTA's barriers to the
 // cluster (a release arrive costs about a microsecond here).
+// The two halves of cluster_sync_relaxed, for a split-phase barrier.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void cluster_sync_relaxed() {
     asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
                  "barrier.cluster.wait.aligned;" ::
