@@ -420,6 +420,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     const uint32_t peer = rank ^ 1u;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
+    // debug build: the page ring (written only by this CTA's own copies; the
+    // exchange buffers, which the peer writes, are left alone)
+    poison_smem(smem, OFF_X);
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     auto FULL = [&](int s) { return BAR(s); };
@@ -618,6 +621,12 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         bool ok = !skip;
         Segment sg;
         while (ok && walk.next(pv, sg)) {
+            // debug build: the piece lies in its unit, in this cluster, and
+            // has a slot exactly when its unit is cut
+            check_split(sg.lp0 >= 0 && sg.lp0 < sg.lp1 && (int64_t)sg.lp1 * PAGE < (int64_t)sg.len + PAGE &&
+                            sg.g_first <= (int)g_id && (int)g_id <= sg.g_last && sg.g_last < (int)launched &&
+                            (sg.slot < 0) == (sg.g_first == sg.g_last) && sg.slot < (int)(launched + U),
+                        0x70);
             for (int64_t lp = sg.lp0; lp < sg.lp1 && ok; ++lp, ++it) {
                 const int s = (int)(it % NSTAGE);
                 ok = mbar_wait(EMPTY(s), (uint32_t)((it / NSTAGE) & 1) ^ 1u, 0x201);
@@ -1201,6 +1210,7 @@ decode_combine_kernel(const Params p) {
         return;
     }
     if (gg.x == gg.y) return;  // written directly by the attention kernel
+    check_split(0 <= gg.x && gg.x < gg.y, 0x71);
     const int n = gg.y - gg.x + 1;
     const int64_t r0 = (int64_t)(gg.x + u) * HEADS + h;  // piece k's row: r0 + k * HEADS
     const float lse_l = lane < n ? p.ws_lse[r0 + (int64_t)lane * HEADS] : -INFINITY;

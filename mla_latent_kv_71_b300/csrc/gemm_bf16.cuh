@@ -295,6 +295,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     while (acc_cols < (uint32_t)(MT * p.BN)) acc_cols <<= 1;
     const uint32_t tmem_cols = 2 * acc_cols;
 
+    poison_smem(smem, (uint32_t)S * stage_bytes + STG_BYTES);  // debug build: ring and staging
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
     const uint32_t accf0 = smem_u32(bars + 2 * S), acce0 = smem_u32(bars + 2 * S + 2);
     const uint32_t fin = smem_u32(bars + 2 * S + 4);
@@ -371,6 +372,13 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                     kc = w.kc0;
                 }
             };
+            // debug build: every item of this CTA lies in the problem
+            for (int i = i0; i < i1; ++i) {
+                const Item c = decode_item(p, i);
+                check_split(c.z < Z && c.nt < p.n_tiles && c.mt + MT <= p.m_tiles && c.kc0 < c.kc1 &&
+                                c.kc1 <= p.K / BK && c.split < p.splits,
+                            0x72);
+            }
             int it = 0;
             for (; item < i1; ++it, next()) {
                 const int s = it % S;

@@ -106,6 +106,8 @@ prefill_bf16_kernel(const __grid_constant__ CUtensorMap tm_kn,   // k_nope [B*L]
     const int nkb = p.causal ? qb + 1 : (p.L + BK - 1) / BK;  // key blocks to visit
     const int64_t tok0 = (int64_t)seq * p.L;                  // the sequence's first token row
 
+    poison_smem(smem, OFF_BAR);  // debug build: the key and value rings
+    check_split(qb >= 0 && q0 < p.L && nkb >= 1 && (int64_t)(nkb - 1) * BK < p.L, 0x73);
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
     auto K_FULL = [&](int s) { return BAR(s); };            // K(j) landed (TMA), stage j % NK

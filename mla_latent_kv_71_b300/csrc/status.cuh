@@ -40,4 +40,36 @@ __device__ __forceinline__ void raise_device_status(uint32_t kind, uint32_t deta
     atomicCAS(&g_device_status, 0u, (kind & 0xFFu) | (detail << 8));
 }
 
+// The debug build (MLA_CHECKS=1, libmla_checks.so) checks each kernel's work
+// split against the shapes: a violated condition raises MLA_DEV_BOUNDS with
+// the given detail (0x7x).  Release builds compile the checks away.
+#ifndef MLA_CHECKS
+#define MLA_CHECKS 0
+#endif
+
+__device__ __forceinline__ void check_split(bool ok, uint32_t detail) {
+#if MLA_CHECKS
+    if (!ok) raise_device_status(MLA_DEV_BOUNDS, detail);
+#else
+    (void)ok;
+    (void)detail;
+#endif
+}
+
+// Debug build: fill `bytes` (a multiple of 16) of shared memory at p with
+// all-ones bytes (NaN as fp32 and bf16) from every thread of the block, then
+// order those writes before any later TMA copy into the same bytes; a read
+// of shared memory that no copy wrote then shows up as NaN in the results.
+// The caller synchronises the block afterwards.
+__device__ __forceinline__ void poison_smem(void* p, uint32_t bytes) {
+#if MLA_CHECKS
+    uint4* q = static_cast<uint4*>(p);
+    for (uint32_t i = threadIdx.x; i < bytes / 16; i += blockDim.x) q[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#else
+    (void)p;
+    (void)bytes;
+#endif
+}
+
 }  // namespace mla

@@ -16,7 +16,10 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmla.so")
+# MLA_CHECKS=1 in the environment selects the build with the kernels' own
+# work-split checks and NaN-filled shared memory (build.py --checks).
+CHECKS = os.environ.get("MLA_CHECKS", "0") == "1"
+LIB_PATH = os.path.join(HERE, "libmla_checks.so" if CHECKS else "libmla.so")
 
 MLA_BF16, MLA_FP32 = 0, 1
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED", 3: "MLA_ERR_CUDA",
@@ -47,8 +50,8 @@ def _lib():
     global _LIB
     if _LIB is None:
         from . import build
-        if build.stale():
-            build.build()
+        if build.stale(CHECKS):
+            build.build(checks=CHECKS)
         lib = ctypes.CDLL(LIB_PATH)
         P, I, L, F, Z = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
                          ctypes.c_size_t)
