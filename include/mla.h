@@ -39,6 +39,15 @@
  *     tensor-core (tcgen05) kernels, fp32 accumulation.  dtype MLA_FP32: fp32
  *     tensors, CUDA-core kernels in fp32.  Shapes the bf16 kernels do not
  *     cover return MLA_ERR_UNSUPPORTED; there is no fallback.
+ *   - The projection GEMMs and the prologue's second kernels are launched
+ *     with programmatic stream serialization: they may start their set-up
+ *     while the kernel before them on the stream finishes, and wait for it
+ *     before touching global memory.  They also let the next kernel launch
+ *     early; a kernel of the caller's launched that way must wait
+ *     (griddepcontrol.wait) before reading what they write.
+ *   - The prefill calls (mla_prefill_*) and the merged-query calls also
+ *     follow from the same pages ([Mishra] "Multi-head Latent Attention":
+ *     the unabsorbed form in training; the fold done once offline).
  */
 #ifndef MLA_H_
 #define MLA_H_
@@ -269,9 +278,8 @@ mla_status_t mla_out_proj_merged(const void* o, const void* w_merged, void* out,
 
 /*
  * Bytes of device workspace mla_cache_append needs (0 for MLA_FP32): the
- * c rows of the N tokens, then the tensor-core GEMM's split-K scratch.  The
- * workspace must be zero-filled before its first use; every call leaves its
- * counters at zero again.
+ * fp32 partial products of the tensor-core GEMM's K splits ([W^DKV ; W^KR] h,
+ * added up by the call's second kernel).  Sized for any d_r <= 128.
  */
 size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype);
 
@@ -289,7 +297,12 @@ size_t mla_cache_append_workspace_size(int N, int d, int d_c, mla_dtype_t dtype)
  * Compression" and "The Positional Problem and Decoupled RoPE".)
  * RoPE rotates pair (x_2k, x_2k+1) by the angle pos * rope_base^(-2k/d_r)
  * (y_2k = x_2k cos - x_2k+1 sin, y_2k+1 = x_2k sin + x_2k+1 cos; the pages
- * fix only that the angle depends on the position), computed in fp64.
+ * fix only that the angle depends on the position).  The angle is kept as
+ * a fraction of a turn: the host passes each frequency as a 64-bit
+ * fixed-point fraction, the kernel multiplies it by the position modulo one
+ * turn in integers and takes fp32 sincospi of the top 24 bits (angle error
+ * below 2^-25 turns for any int32 position; no fp64 on the device).
+ * d_r <= 128.
  *
  *   h          [N, d]                   hidden states of the new tokens
  *   w_dkv      [d_c, d]                 W^DKV
@@ -318,8 +331,9 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
                               mla_dtype_t dtype, mla_stream_t stream);
 
 /*
- * Bytes of device workspace mla_project_q needs (0 for MLA_FP32); same
- * zero-fill rule as mla_cache_append_workspace_size.
+ * Bytes of device workspace mla_project_q needs (0 for MLA_FP32): the fp32
+ * partial products of the GEMM's K splits, added up by the call's second
+ * kernel.
  */
 size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype);
 
@@ -328,8 +342,7 @@ size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_d
  *     q = W^Q h_n;  head i takes rows i*(d_h+d_r) .. (i+1)*(d_h+d_r)-1,
  *     the first d_h as q^C_i (-> q_nope), the last d_r as q^R_i, which is
  *     rotated at position pos_n (-> q_pe), with the RoPE of mla_cache_append
- *     (in bf16 the sine and cosine of each angle, taken in fp64, are kept as
- *     fp32 and the rotation is done in fp32).
+ *     (the rotation in fp32; each value rounded once to the output type).
  * ([llms] "The Positional Problem and Decoupled RoPE": each head's query is
  * the concatenation [q^C ; q^R] and only q^R is rotated; [Mishra] "Step 4:
  * decoupled RoPE".)  h may be the model's hidden state (one W^Q) or the
@@ -341,7 +354,7 @@ size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_d
  *   q_nope    [N, H, d_h]               output, the content query q^C
  *   q_pe      [N, H, d_r]               output, the rotated RoPE query
  *   workspace >= mla_project_q_workspace_size(N, H, d_h, d_r, d, dtype)
- * d_r even (MLA_ERR_INVALID_ARG otherwise); d_h even; bf16:
+ * d_r even (MLA_ERR_INVALID_ARG otherwise); d_h even, d_r <= 128; bf16:
  * H*(d_h+d_r) % 128 == 0, d % 64 == 0, d_h % 8 == 0, d_r % 8 == 0;
  * fp32: d % 4 == 0.
  */
