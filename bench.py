@@ -204,9 +204,10 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def traffic_record(kernel_src_sha: str):
+def traffic_record(kernel_src_sha: str, workload: str):
     """DRAM bytes per launch of the attention kernel from a committed ncu
-    capture, or None if absent or taken on a different kernel source."""
+    capture, or None if absent, taken on a different kernel source, or on a
+    different workload."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.json")
     if not os.path.exists(path):
         return None, None
@@ -214,6 +215,8 @@ def traffic_record(kernel_src_sha: str):
         d = json.load(f)
     if d.get("kernel_src_sha256") != kernel_src_sha:
         return None, "stale"
+    if d.get("workload") != workload:
+        return None, "other workload"
     return d.get("dram_bytes_per_launch"), d.get("source")
 
 
@@ -359,10 +362,15 @@ def run_ours(args, rank, world, local):
     rep_ms = [a.elapsed_time(b) for a, b in ev_rep]
     step_ms = statistics.median(rep_ms) / args.steps
     step_ms = max_over_ranks(step_ms, world)
-    with torch.cuda.stream(s):
-        graph_ev.replay()
-    torch.cuda.synchronize(dev)
-    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in ev_attn)
+    # the attention kernel's own time: the median over the K steps of the
+    # events around it, from three replays of the events graph
+    attn_samples = []
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            graph_ev.replay()
+        torch.cuda.synchronize(dev)
+        attn_samples += [a.elapsed_time(b) for a, b in ev_attn]
+    attn_ms = statistics.median(attn_samples)
     code, detail = mla.get_device_status()
     if code != 0:
         raise RuntimeError(f"device status {code} detail {detail:#x}")
@@ -430,7 +438,7 @@ def run_ours(args, rank, world, local):
     t_flop = flops / (pk["bf16_tflops"] * 1e12)
     t_hbm = cache_bytes / (pk["hbm_gbs"] * 1e9)
     attn_s = attn_ms * 1e-3
-    traffic, _ = traffic_record(kernel_sha())
+    traffic, _ = traffic_record(kernel_sha(), args.workload)
     if t_hbm >= t_flop:
         roof = {"bound": "hbm", "achieved": cache_bytes / attn_s / 1e9, "peak": pk["hbm_gbs"],
                 "unit": "GB/s"}
