@@ -14,8 +14,9 @@
 // Layout on the chip.  O alone (128 x 512 fp32) fills a whole SM's TMEM, so
 // a cluster of two CTAs splits the feature axis: CTA r owns latent columns
 // 256r .. 256r+255 and RoPE columns 32r .. 32r+31 (288 of the 576 features).
-// Each CTA loads only its half of every 64-token page (36 KB: one TMA box
-// per 64 columns), computes a partial S over its 288 features, and the two
+// Each CTA loads only its half of every 64-token page (36 KB, as two 32-token
+// tiles of one TMA box per 64 columns), computes a partial S over its 288
+// features, and the two
 // partial S tiles are exchanged through distributed shared memory.  Both
 // CTAs then run the identical softmax and accumulate their own 256 columns
 // of O.  Every cache byte is read from HBM once and no tensor work is
@@ -38,15 +39,22 @@
 // front half of the next); its P goes to buffer i % 2.  The latent Q and P
 // are UMMA A operands read from TMEM; the RoPE part of Q (128 x 32) sits in
 // shared memory and feeds the two RoPE steps of S as an SS product.  The
-// page in shared memory is the B operand of both products: K-major for S
-// (features contiguous), MN-major for O (the same bytes, read along the
-// feature axis).
+// tile's rows in shared memory are the B operand of both products: K-major
+// for S (features contiguous), MN-major for O (the same bytes, read along
+// the feature axis).
+//
+// The ring holds eight tiles (half pages), each stage released as soon as
+// its own tile's O product is done: with whole pages as stages a page's
+// first tile kept its bytes until the second tile's product, and the ring's
+// depth in flight is what paces the steady state (a tile lives ~9,000
+// cycles from its copy's issue to its release).
 //
 // Warp roles (352 threads):
-//   warp 0      TMA producer: pages into a 4-stage ring (and zeroes the rows
-//               past the end of a partial last page),
+//   warp 0      TMA producer: tiles into the 8-stage ring, one page-table
+//               read per page (and zeroes the rows past the end of a
+//               partial last tile),
 //   warp 1      TMEM owner; an elected lane issues each tile's S = Q.K^T as
-//               soon as its page has landed and its S buffer is free,
+//               soon as its tile has landed and its S buffer is free,
 //   warp 2      an elected lane issues each tile's O += P.C, in tile order,
 //               as soon as its P is in TMEM,
 //   warps 3..6  tiles 0, 2, 4, ...: partial S -> peer, peer's partial ->
@@ -85,16 +93,16 @@ constexpr int DR = 64;         // RoPE key width
 constexpr int HALF_C = 256;    // latent columns per CTA
 constexpr int HALF_R = 32;     // RoPE columns per CTA
 constexpr int HEADS = 128;     // heads per unit (UMMA M)
-constexpr int NSTAGE = 4;      // page pipeline depth
+constexpr int NHS = 8;         // ring depth in half pages (one 32-token tile each)
 constexpr int THREADS = 352;
 constexpr int WG_WARP0 = 3;    // warps 3..6: tiles with even index, 7..10: odd
 
-constexpr uint32_t BOX_C_BYTES = PAGE * 128;                      // 64 rows x 64 bf16
-constexpr uint32_t BOX_R_BYTES = PAGE * 64;                       // 64 rows x 32 bf16
-constexpr uint32_t STAGE_BYTES = 4 * BOX_C_BYTES + BOX_R_BYTES;   // 36864
+constexpr uint32_t HBOX_C_BYTES = TILE * 128;                      // 32 rows x 64 bf16
+constexpr uint32_t HBOX_R_BYTES = TILE * 64;                       // 32 rows x 32 bf16
+constexpr uint32_t HSTAGE_BYTES = 4 * HBOX_C_BYTES + HBOX_R_BYTES;  // 18432: one tile of a CTA's half
 constexpr uint32_t XT_BYTES = HEADS * TILE * 4;                   // one partial S tile, fp32
 constexpr uint32_t OFF_STAGE = 0;
-constexpr uint32_t OFF_X = NSTAGE * STAGE_BYTES;    // the peer's partial S tiles [group][slot]
+constexpr uint32_t OFF_X = NHS * HSTAGE_BYTES;      // the peer's partial S tiles [group][slot]
 constexpr uint32_t OFF_PUB = OFF_X + 4 * XT_BYTES;  // per-row state handed between the groups
 constexpr uint32_t PUB_BYTES = 2 * 4 * HEADS * 4;      // [2 parities][m_used, m_ref, l_part, lr_part][128]
 // This CTA's 32 RoPE columns of the query (128 rows x 64 B, the layout a
@@ -102,7 +110,7 @@ constexpr uint32_t PUB_BYTES = 2 * 4 * HEADS * 4;      // [2 parities][m_used, m
 constexpr uint32_t OFF_QPE = OFF_PUB + PUB_BYTES;      // 1 KB aligned
 constexpr uint32_t QPE_BYTES = HEADS * HALF_R * 2;
 constexpr uint32_t OFF_BAR = OFF_QPE + QPE_BYTES;
-constexpr uint32_t NUM_BARS = 35;
+constexpr uint32_t NUM_BARS = 43;
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_BYTES + 1024;  // slack for 1 KB alignment
@@ -373,8 +381,10 @@ struct TileIter {
     __device__ bool first_in_seg() const { return lp == sg.lp0 && t == 0; }
     __device__ bool last_in_page() const { return t + 1 == ntp; }
     __device__ bool last_in_seg() const { return last_in_page() && lp + 1 == sg.lp1; }
-    __device__ int stage() const { return (int)(page % NSTAGE); }
-    __device__ uint32_t page_parity() const { return (uint32_t)((page / NSTAGE) & 1); }
+    // ring stage of this tile (the half page it lies in) and the parity of
+    // its phase of that stage's barriers
+    __device__ int hstage() const { return tile % NHS; }
+    __device__ uint32_t hparity() const { return (uint32_t)((tile / NHS) & 1); }
     __device__ int sbuf() const { return tile % NS; }  // TMEM partial S buffer
     // parity of the phase of an S-buffer barrier for the tile n back
     __device__ uint32_t s_parity(int back = 0) const { return (uint32_t)(((tile - back) / NS) & 1); }
@@ -390,12 +400,9 @@ struct BoolC {
 
 // What a tile group keeps of a tile between its two halves of work.
 struct TileInfo {
-    int tile, seg, u, slot, g_first, g_last, valid, stage, tp;
-    bool first, last, last_in_page;
+    int tile, seg, u, slot, g_first, g_last, valid;
+    bool first, last;
     __device__ void set(const TileIter& it) {
-        stage = it.stage();
-        tp = it.t;
-        last_in_page = it.last_in_page();
         tile = it.tile;
         seg = it.seg;
         u = it.sg.u;
@@ -425,8 +432,9 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     poison_smem(smem, OFF_X);
     const uint32_t bar0 = smem_u32(smem + OFF_BAR);
     auto BAR = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-    auto FULL = [&](int s) { return BAR(s); };
-    auto EMPTY = [&](int s) { return BAR(NSTAGE + s); };
+    // ring stage h (a half page): landed (TMA bytes), released (commit)
+    auto FULL = [&](int h) { return h < 4 ? BAR(h) : BAR(35 + (h - 4)); };
+    auto EMPTY = [&](int h) { return h < 4 ? BAR(4 + h) : BAR(39 + (h - 4)); };
     // Tile i's partial S is in S buffer i % 3 (the k-th use of a buffer is
     // phase k of its barriers), its P in P buffer i % 2.
     auto S_FULL = [&](int k) { return BAR(8 + k); };    // partial S of the buffer's tile (commit)
@@ -440,13 +448,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
     auto L_PUB = [&](int b) { return BAR(28 + b); };    // group's row sums after the tile (4 warps)
     const uint32_t Q_FULL = BAR(30);                    // query of a unit in TMEM + smem (4 warps)
     const uint32_t O_FREE = BAR(31);                    // epilogue read O (4 warps)
-    const uint32_t TAIL = BAR(32);                      // partial last page landed (TMA)
+    const uint32_t TAIL = BAR(32);                      // partial last tile landed (TMA)
     auto DRAIN = [&](int k) { return BAR(33 + k); };    // teardown: MMAs of warp 1 + k finished
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
     int64_t* misc = reinterpret_cast<int64_t*>(smem + OFF_MISC + 8);
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
+        for (int s = 0; s < NHS; ++s) {
             mbar_init(FULL(s), 1);
             mbar_init(EMPTY(s), 1);
         }
@@ -627,57 +635,63 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                             sg.g_first <= (int)g_id && (int)g_id <= sg.g_last && sg.g_last < (int)launched &&
                             (sg.slot < 0) == (sg.g_first == sg.g_last) && sg.slot < (int)(launched + U),
                         0x70);
-            for (int64_t lp = sg.lp0; lp < sg.lp1 && ok; ++lp, ++it) {
-                const int s = (int)(it % NSTAGE);
-                ok = mbar_wait(EMPTY(s), (uint32_t)((it / NSTAGE) & 1) ^ 1u, 0x201);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
+            for (int64_t lp = sg.lp0; lp < sg.lp1 && ok; ++lp) {
                 const int b_seq = sg.u % p.B;  // unit u = (t * HG + hg) * B + b
                 int64_t pg = p.page_table[(int64_t)b_seq * p.max_pages + lp];
                 if (pg < 0 || pg >= p.num_pages) {
                     raise_device_status(MLA_DEV_BOUNDS, 0x20);
                     pg = 0;
                 }
-                const int y = (int)(pg * PAGE);
                 const int valid = page_valid(sg, lp);
-                const uint32_t st = smem_u32(smem + OFF_STAGE + s * STAGE_BYTES);
-                const uint32_t bar = valid == PAGE ? FULL(s) : TAIL;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bar, STAGE_BYTES);
-                    for (int k = 0; k < 4; ++k)
-                        tma_load_2d(st + k * BOX_C_BYTES, &tm_c, bar, (int)rank * HALF_C + 64 * k,
-                                    y, pol);
-                    tma_load_2d(st + 4 * BOX_C_BYTES, &tm_r, bar, DC + (int)rank * HALF_R, y, pol);
-                }
-                if (valid < PAGE) {
-                    // Rows past the end may hold anything (even NaN); zero
-                    // them so that P = 0 there cannot meet a NaN in P . C.
-                    // (The copy was issued here, so it is waited for even
-                    // when another CTA has raised the status word.)
-                    ok = mbar_wait_teardown(TAIL, tail_phase, MLA_WAIT_LIMIT_NS);
+                const int ntp = valid > TILE ? 2 : 1;  // the tiles the consumers take from this page
+                // Each tile of the page has its own ring stage (half a page),
+                // so a stage goes back to the ring as soon as its tile's
+                // O product is done, not its page's second tile's.
+                for (int t = 0; t < ntp && ok; ++t, ++it) {
+                    const int h = (int)(it % NHS);
+                    ok = mbar_wait(EMPTY(h), (uint32_t)((it / NHS) & 1) ^ 1u, 0x201);
                     ok = __all_sync(0xffffffffu, ok);
-                    tail_phase ^= 1u;
-                    if (!ok) {
-                        raise_device_status(MLA_DEV_TIMEOUT, 0x202u | ((blockIdx.x & 0xFFFu) << 12));
-                        ++it;
-                        break;
+                    if (!ok) break;
+                    const int y = (int)(pg * PAGE) + t * TILE;
+                    const int vt = min(TILE, valid - t * TILE);  // visible rows of this tile
+                    const uint32_t st = smem_u32(smem + OFF_STAGE + h * HSTAGE_BYTES);
+                    const uint32_t bar = vt == TILE ? FULL(h) : TAIL;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(bar, HSTAGE_BYTES);
+                        for (int k = 0; k < 4; ++k)
+                            tma_load_2d(st + k * HBOX_C_BYTES, &tm_c, bar, (int)rank * HALF_C + 64 * k, y, pol);
+                        tma_load_2d(st + 4 * HBOX_C_BYTES, &tm_r, bar, DC + (int)rank * HALF_R, y, pol);
                     }
-                    uint8_t* tile = smem + OFF_STAGE + s * STAGE_BYTES;
-                    const int rows = PAGE - valid;
-                    for (int idx = lane; idx < rows * 8 * 4; idx += 32) {  // latent boxes
-                        const int box = idx / (rows * 8), rem = idx % (rows * 8);
-                        uint4* dst = reinterpret_cast<uint4*>(tile + box * BOX_C_BYTES +
-                                                              (valid + rem / 8) * 128 + (rem % 8) * 16);
-                        *dst = make_uint4(0u, 0u, 0u, 0u);
+                    if (vt < TILE) {
+                        // Rows past the end may hold anything (even NaN); zero
+                        // them so that P = 0 there cannot meet a NaN in P . C.
+                        // (The copy was issued here, so it is waited for even
+                        // when another CTA has raised the status word.)
+                        ok = mbar_wait_teardown(TAIL, tail_phase, MLA_WAIT_LIMIT_NS);
+                        ok = __all_sync(0xffffffffu, ok);
+                        tail_phase ^= 1u;
+                        if (!ok) {
+                            raise_device_status(MLA_DEV_TIMEOUT, 0x202u | ((blockIdx.x & 0xFFFu) << 12));
+                            ++it;
+                            break;
+                        }
+                        uint8_t* tile = smem + OFF_STAGE + h * HSTAGE_BYTES;
+                        const int rows = TILE - vt;
+                        for (int idx = lane; idx < rows * 8 * 4; idx += 32) {  // latent boxes
+                            const int box = idx / (rows * 8), rem = idx % (rows * 8);
+                            uint4* dst = reinterpret_cast<uint4*>(tile + box * HBOX_C_BYTES +
+                                                                  (vt + rem / 8) * 128 + (rem % 8) * 16);
+                            *dst = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        for (int idx = lane; idx < rows * 4; idx += 32) {  // RoPE box
+                            uint4* dst = reinterpret_cast<uint4*>(tile + 4 * HBOX_C_BYTES +
+                                                                  (vt + idx / 4) * 64 + (idx % 4) * 16);
+                            *dst = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(FULL(h));
                     }
-                    for (int idx = lane; idx < rows * 4; idx += 32) {  // RoPE box
-                        uint4* dst = reinterpret_cast<uint4*>(tile + 4 * BOX_C_BYTES +
-                                                              (valid + idx / 4) * 64 + (idx % 4) * 16);
-                        *dst = make_uint4(0u, 0u, 0u, 0u);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(FULL(s));
                 }
             }
         }
@@ -686,8 +700,8 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         // an abort alike.  A partial page's FULL phase is this warp's own
         // arrive, made above once its copy had landed.  (The tensor core's
         // releases of the ring are waited for by the MMA warps themselves.)
-        for (int64_t i = (it > NSTAGE ? it - NSTAGE : 0); i < it; ++i)
-            mbar_wait_teardown(FULL((int)(i % NSTAGE)), (uint32_t)((i / NSTAGE) & 1), MLA_WAIT_LIMIT_NS);
+        for (int64_t i = (it > NHS ? it - NHS : 0); i < it; ++i)
+            mbar_wait_teardown(FULL((int)(i % NHS)), (uint32_t)((i / NHS) & 1), MLA_WAIT_LIMIT_NS);
     } else if (warp == 1) {
         // ========================================================= MMA: S
         // The score products S = Q.K^T, tile by tile, each as soon as its
@@ -699,11 +713,11 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         bool ok = !skip;
         bool issued = false;
         const uint64_t dq0 = smem_desc(smem_u32(smem + OFF_STAGE), 16, 1024, SWZ_128B);
-        const uint64_t dr0 = smem_desc(smem_u32(smem + OFF_STAGE + 4 * BOX_C_BYTES), 16, 512, SWZ_64B);
+        const uint64_t dr0 = smem_desc(smem_u32(smem + OFF_STAGE + 4 * HBOX_C_BYTES), 16, 512, SWZ_64B);
         const uint64_t dqpe = smem_desc(smem_u32(smem + OFF_QPE), 16, 512, SWZ_64B);
         while (ok && qk.have) {
             const int k3 = qk.sbuf();
-            if (qk.t == 0) ok = __all_sync(0xffffffffu, mbar_wait(FULL(qk.stage()), qk.page_parity(), 0x301));
+            ok = __all_sync(0xffffffffu, mbar_wait(FULL(qk.hstage()), qk.hparity(), 0x301));
             // the softmax has re-read the buffer's last tile (three back)
             if (ok && qk.tile >= NS) ok = __all_sync(0xffffffffu, mbar_wait(S_FREE(k3), qk.s_parity(NS), 0x302));
             if (ok && qk.first_in_seg())
@@ -711,13 +725,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             if (!ok) break;
             tc_fence_after();
             if (elect_one_sync()) {
-                const uint32_t off = (uint32_t)(qk.stage() * STAGE_BYTES);
-                const uint64_t dc = dq0 + ((uint64_t)(off + qk.t * (TILE * 128)) >> 4);
-                const uint64_t dr = dr0 + ((uint64_t)(off + qk.t * (TILE * 64)) >> 4);
+                const uint32_t off = (uint32_t)(qk.hstage() * HSTAGE_BYTES);
+                const uint64_t dc = dq0 + ((uint64_t)off >> 4);
+                const uint64_t dr = dr0 + ((uint64_t)off >> 4);
                 const uint32_t d = tmem + TM_S + 32 * k3;
 #pragma unroll
                 for (int k = 0; k < 16; ++k)  // latent features, K-major SW128
-                    mma_ts(d, tmem + TM_Q + 8 * k, dc + (uint64_t)(((k / 4) * BOX_C_BYTES + (k % 4) * 32) >> 4),
+                    mma_ts(d, tmem + TM_Q + 8 * k, dc + (uint64_t)(((k / 4) * HBOX_C_BYTES + (k % 4) * 32) >> 4),
                            IDESC_QK, k > 0 ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < 2; ++k)  // RoPE features, both operands K-major SW64 in smem
@@ -744,7 +758,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
         it.begin(walk, pv);
         bool ok = !skip;
         bool issued = false;
-        const uint64_t dp0 = smem_desc(smem_u32(smem + OFF_STAGE), BOX_C_BYTES, 1024, SWZ_128B);
+        const uint64_t dp0 = smem_desc(smem_u32(smem + OFF_STAGE), HBOX_C_BYTES, 1024, SWZ_128B);
         while (ok && it.have) {
             const int b = it.buf();
             ok = __all_sync(0xffffffffu, mbar_wait(P_FULL(b), it.parity(), 0x401));
@@ -755,14 +769,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
             if (elect_one_sync()) {
                 // C as MN-major B: 64-column boxes 8 KB apart, 8-row
                 // groups 1 KB apart, 16 tokens = 2 KB per step.
-                const uint64_t db = dp0 + ((uint64_t)(it.stage() * STAGE_BYTES + it.t * (TILE * 128)) >> 4);
+                const uint64_t db = dp0 + ((uint64_t)(it.hstage() * HSTAGE_BYTES) >> 4);
                 const uint32_t acc0 = it.first_in_seg() ? 0u : 1u;
 #pragma unroll
                 for (int k = 0; k < TILE / 16; ++k)
                     mma_ts(tmem + TM_O, tmem + TM_P + 16 * b + 8 * k, db + (uint64_t)(k * 2048 >> 4), IDESC_PV,
                            k == 0 ? acc0 : 1u);
                 tc_commit(PV_DONE(b));
-                if (it.last_in_page()) tc_commit(EMPTY(it.stage()));
+                tc_commit(EMPTY(it.hstage()));
             }
             __syncwarp();
             issued = true;

@@ -1056,8 +1056,9 @@ mla_status_t decode_impl(const void* q_lat, const void* q_pe, const void* kv_poo
     CUtensorMap tm_c, tm_r;
     const cuuint64_t dims[2] = {(cuuint64_t)(d_c + d_r), (cuuint64_t)num_pages * page_size};
     const cuuint64_t strides[1] = {(cuuint64_t)(d_c + d_r) * 2};
-    const cuuint32_t box_c[2] = {64, (cuuint32_t)page_size};
-    const cuuint32_t box_r[2] = {(cuuint32_t)mla::dec::HALF_R, (cuuint32_t)page_size};
+    // one 32-token tile of a page per copy: the ring holds half pages
+    const cuuint32_t box_c[2] = {64, (cuuint32_t)mla::dec::TILE};
+    const cuuint32_t box_r[2] = {(cuuint32_t)mla::dec::HALF_R, (cuuint32_t)mla::dec::TILE};
     if (!make_map(&tm_c, kv_pool, 2, dims, strides, box_c, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_r, kv_pool, 2, dims, strides, box_r, CU_TENSOR_MAP_SWIZZLE_64B))
         return MLA_ERR_CUDA;
