@@ -21,6 +21,21 @@ int main(void) {
         MLA_ERR_INVALID_ARG)
         ++fails;
     if (mla_decode_workspace_size(0, 1, 128, 512, MLA_BF16) != 0) ++fails;
+    {   /* RoPE widths past 128 are refused before any device work (the
+         * pointers are never touched: they only have to be aligned) */
+        void* fake = (void*)(size_t)4096;
+        const int32_t* ifake = (const int32_t*)fake;
+        if (mla_cache_append(fake, fake, fake, ifake, ifake, ifake, fake, 1, 64, 16, 130, 1, 64, 1, 1,
+                             10000.0, NULL, 0, MLA_FP32, NULL) != MLA_ERR_UNSUPPORTED)
+            ++fails;
+        if (mla_project_q(fake, fake, ifake, fake, fake, 1, 1, 32, 130, 64, 10000.0, NULL, 0, MLA_FP32,
+                          NULL) != MLA_ERR_UNSUPPORTED)
+            ++fails;
+        /* odd RoPE widths have no pairs */
+        if (mla_project_q(fake, fake, ifake, fake, fake, 1, 1, 32, 15, 64, 10000.0, NULL, 0, MLA_FP32,
+                          NULL) != MLA_ERR_INVALID_ARG)
+            ++fails;
+    }
     printf(fails ? "FAIL %d\n" : "ok\n", fails);
     return fails != 0;
 }
