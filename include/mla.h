@@ -331,9 +331,12 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
                               mla_dtype_t dtype, mla_stream_t stream);
 
 /*
- * Bytes of device workspace mla_project_q needs (0 for MLA_FP32): the fp32
- * partial products of the GEMM's K splits, added up by the call's second
- * kernel.
+ * Bytes of device workspace mla_project_q needs.  0 for MLA_FP32, and 0 in
+ * bf16 when the GEMM's 128-row output tiles alone give at least half of the
+ * SMs work (H*(d_h+d_r) = 24576 at DeepSeek widths): its epilogue then splits
+ * the rows per head and rotates q^R itself, in one launch.  Otherwise (few
+ * heads, a long d) the fp32 partial products of the GEMM's K splits, added
+ * up by the call's second kernel.
  */
 size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype);
 

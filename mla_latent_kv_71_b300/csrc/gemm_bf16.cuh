@@ -32,7 +32,10 @@
 // each split's fp32 partial goes to the workspace, and the last CTA to finish
 // a tile adds the splits in split order and writes bf16), OUT_PARTS (every
 // split's fp32 partial to the workspace, added up by the caller's next
-// kernel, which also applies its own epilogue).
+// kernel, which also applies its own epilogue), OUT_QROPE (no split: D is
+// the stacked per-head query W^Q h; each row goes to its head's q^C or q^R,
+// and the q^R pairs are rotated at their token's position before the one
+// rounding to bf16).
 #pragma once
 
 #include <cstdint>
@@ -41,6 +44,7 @@
 
 #include "pdl.cuh"
 #include "ptx.cuh"
+#include "rope.cuh"
 #include "status.cuh"
 #include "tmem_batch.cuh"
 
@@ -55,9 +59,16 @@ constexpr int EPI_WARP0 = 2;
 constexpr int A_BYTES = BM * BK * 2;            // 16 KB per stage
 constexpr int EPI_COLS = 64;                    // accumulator columns staged per round
 constexpr int STG_BYTES = EPI_COLS * BM * 4;    // 32 KB (fp32 rows of 128)
+constexpr int CTL_BYTES = 256;                  // barriers, TMEM address, reducer flag
+constexpr int FREQ_BYTES = rope::MAX_PAIRS * 8; // OUT_QROPE: the RoPE frequencies
+constexpr int POS_BYTES = 256 * 4;              // OUT_QROPE: positions of an N tile's tokens
+// shared memory besides the ring: 1 KB alignment slack, staging, control,
+// frequencies, positions
+constexpr int FIXED_SMEM = 1024 + STG_BYTES + CTL_BYTES + FREQ_BYTES + POS_BYTES;
+static_assert((2 * MAX_STAGES + 5) * 8 + 8 <= CTL_BYTES, "barriers, TMEM address and flag fit");
 constexpr uint32_t SMEM_CAP = 227 * 1024;
 
-enum : int { OUT_BF16 = 0, OUT_REDUCE = 1, OUT_PARTS = 2 };
+enum : int { OUT_BF16 = 0, OUT_REDUCE = 1, OUT_PARTS = 2, OUT_QROPE = 3 };
 
 struct Params {
     int M;                // rows of D that exist (a multiple of 8; the last M tile may be partial)
@@ -73,13 +84,23 @@ struct Params {
     int chunks_per_split; // K chunks (of BK) per split; the last split may be shorter
     int items;            // Z * n_tiles * splits * m_units
     int stages;           // TMA ring depth, 1..MAX_STAGES
-    int mode;             // OUT_BF16 / OUT_REDUCE / OUT_PARTS
+    int mode;             // OUT_BF16 / OUT_REDUCE / OUT_PARTS / OUT_QROPE
     int a_evict_first;    // A is read once (one N tile): let it leave L2 first
     int vec_out;          // out, ldo and out_z allow 16-byte stores
     __nv_bfloat16* out;   // out[(n0+n) * ldo + z * out_z + m]
     int64_t ldo, out_z;
     float* ws_part;       // [splits][Z][N][M] fp32 partials (OUT_REDUCE, OUT_PARTS)
     int* ws_count;        // [Z * n_tiles * m_tiles] arrival counters (OUT_REDUCE), zero between calls
+    // OUT_QROPE: row m of D is row f = m % (d_h + d_r) of query head
+    // i = m / (d_h + d_r); f < d_h goes to q_nope[n][i][f], the rest, pair
+    // (f - d_h, f - d_h + 1) rotated at positions[n] with frequency
+    // freq[(f - d_h) / 2] (rope.cuh), to q_pe[n][i][f - d_h].  d_h and d_r
+    // are multiples of 8, so an 8-row piece of a tile lies in one part.
+    __nv_bfloat16* q_nope;
+    __nv_bfloat16* q_pe;
+    const int32_t* positions;
+    int q_heads, d_h, d_r;
+    uint64_t freq[rope::MAX_PAIRS];
 };
 
 struct Item {
@@ -123,18 +144,23 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 
 // One M tile of an item's accumulator (TMEM columns 0..BN of `tacc`, this
 // thread's lane quarter already added) to global memory: bf16 rows of `out`,
-// or this split's fp32 rows of the partials.  Runs in the 128 epilogue
+// this split's fp32 rows of the partials (fp32), or the query heads
+// (OUT_QROPE, staged in fp32 so that the rotation precedes the rounding).
+// Runs in the 128 epilogue
 // threads (t = 0..127, row = t in the tile); 64 columns per round through
 // `stg`.  When release != 0 the TMEM buffer is handed back (one arrival per
 // warp on that barrier) as soon as the last round's columns are in
 // registers.
 __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int mt, int Z, uint32_t tacc,
-                                           uint8_t* stg, int t, bool fp32, uint32_t release) {
+                                           uint8_t* stg, const uint64_t* freq, const int32_t* pos_s, int t,
+                                           bool fp32, uint32_t release) {
     const int m0 = mt * BM, n0 = w.nt * p.BN;
     const int n_valid = min(p.BN, p.N - n0);
     const int mv = min(BM, p.M - m0);
     float* stg_f = reinterpret_cast<float*>(stg);
     uint16_t* stg_h = reinterpret_cast<uint16_t*>(stg);
+    const bool qrope = p.mode == OUT_QROPE;
+    const bool stage32 = fp32 || qrope;
     for (int c0 = 0; c0 < n_valid; c0 += EPI_COLS) {
         uint32_t r[64];
         const bool two = c0 + 32 < n_valid;
@@ -148,7 +174,7 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
             if ((t & 31) == 0) mbar_arrive(release);
         }
         const int nj = two ? 64 : 32;
-        if (fp32) {
+        if (stage32) {
 #pragma unroll
             for (int j = 0; j < 64; ++j)
                 if (j < nj) stg_f[j * BM + t] = __uint_as_float(r[j]);
@@ -170,6 +196,39 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
                     *reinterpret_cast<float4*>(base + (int64_t)j * p.M + m) =
                         *reinterpret_cast<const float4*>(stg_f + j * BM + m);
             }
+        } else if (qrope) {
+            // 8 rows (one 16-byte store) of one token per step.  Thread t
+            // always takes rows 8 (t % 16) .. +7 of the tile (BM is a
+            // multiple of 16), so its head, part and frequencies are fixed
+            // for the tile and only the token changes.
+            const int m = (t & 15) * 8;
+            const int qw = p.d_h + p.d_r, row = m0 + m;
+            const int i = row / qw, f = row - i * qw;
+            const bool rot = f >= p.d_h;
+            uint64_t fr[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) fr[k] = rot ? freq[(f - p.d_h) / 2 + k] : 0;
+            __nv_bfloat16* dst0 = rot ? p.q_pe + (int64_t)i * p.d_r + (f - p.d_h) : p.q_nope + (int64_t)i * p.d_h + f;
+            const int64_t tok_stride = (int64_t)p.q_heads * (rot ? p.d_r : p.d_h);
+            if (m < mv)
+                for (int j = t >> 4; j < ncols; j += BM / 16) {
+                    const int n = n0 + c0 + j;
+                    const float4 lo = *reinterpret_cast<const float4*>(stg_f + j * BM + m);
+                    const float4 hi = *reinterpret_cast<const float4*>(stg_f + j * BM + m + 4);
+                    float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                    if (rot) {
+                        const int64_t pos = pos_s[j + c0];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            float sn, cs;
+                            rope::rope_sincos(pos, fr[k], sn, cs);
+                            rope::rotate(v[2 * k], v[2 * k + 1], sn, cs, v[2 * k], v[2 * k + 1]);
+                        }
+                    }
+                    *reinterpret_cast<uint4*>(dst0 + n * tok_stride) =
+                        make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
+                                   pack2_bf16(v[6], v[7]));
+                }
         } else {
             __nv_bfloat16* base = p.out + (int64_t)(n0 + c0) * p.ldo + (int64_t)w.z * p.out_z + m0;
             for (int idx = t; idx < ncols * 16; idx += BM) {
@@ -264,6 +323,8 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     // bars: [0, S) full, [S, 2S) empty, 2S + b acc_full, 2S + 2 + b acc_empty, 2S + 4 final
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
     int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] this tile's reducer
+    uint64_t* freq_s = reinterpret_cast<uint64_t*>(stg + STG_BYTES + CTL_BYTES);
+    int32_t* pos_s = reinterpret_cast<int32_t*>(stg + STG_BYTES + CTL_BYTES + FREQ_BYTES);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int i0 = (int)((int64_t)p.items * blockIdx.x / gridDim.x);
@@ -288,6 +349,10 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         }
         mbar_init(fin, 1);
         flag[0] = 0;
+        // the frequencies in shared memory: the epilogue's threads index
+        // them by row, which the constant bank would serialise
+        if (p.mode == OUT_QROPE)
+            for (int k = 0; k < rope::MAX_PAIRS; ++k) freq_s[k] = p.freq[k];
         fence_mbar_init_cluster();
     }
     if (warp == 0 && lane == 0) {
@@ -419,10 +484,17 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         const int q = warp & 3;
         const int t = q * 32 + lane;  // row of the tile this thread reads from TMEM
         bool ok = true;
-        int acc = 0;
+        int acc = 0, pos_nt = -1;
         for (int item = i0; item < i1; ++item, ++acc) {
             const Item w = decode_item(p, item);
             const uint32_t b = acc & 1, use = acc >> 1;
+            if (p.mode == OUT_QROPE && w.nt != pos_nt) {
+                // the N tile's token positions, read while the products run
+                // (the previous item's stores, which read them, are done)
+                pos_nt = w.nt;
+                for (int j = t; j < p.BN; j += BM)
+                    pos_s[j] = w.nt * p.BN + j < p.N ? __ldg(p.positions + w.nt * p.BN + j) : 0;
+            }
             bool good = ok && __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * b, use & 1, 0x104));
             good = epi_sync_and(good);
             ok = good;
@@ -433,7 +505,8 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                 // the last tile's final TMEM read hands the buffer back
                 if (good)
                     store_tile(p, w, mt, Z, tmem + b * acc_cols + (uint32_t)(j * p.BN) + ((uint32_t)(q * 32) << 16),
-                               stg, t, p.mode != OUT_BF16, j == MT - 1 ? acce0 + 8 * b : 0u);
+                               stg, freq_s, pos_s, t, p.mode == OUT_REDUCE || p.mode == OUT_PARTS,
+                               j == MT - 1 ? acce0 + 8 * b : 0u);
                 if (p.mode == OUT_REDUCE) {
                     // Every CTA of a split tile arrives on its counter -- also
                     // one that gave up -- and the last arrival resets it, so

@@ -297,7 +297,7 @@ GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max
     g.items = items > 0x7FFFFFFF ? 0 : (int)items;  // 0: too large (refused by the caller)
     g.grid = (int)std::min<int64_t>(items, sms);
     const size_t stage = (size_t)g.MT * mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
-    const size_t fixed = 1024 + mla::gemm::STG_BYTES + 256;
+    const size_t fixed = mla::gemm::FIXED_SMEM;
     g.stages = (int)std::min<size_t>(mla::gemm::MAX_STAGES, (mla::gemm::SMEM_CAP - fixed) / stage);
     g.smem = fixed + (size_t)g.stages * stage;
     g.ws_part_bytes = g.mode != mla::gemm::OUT_BF16 ? sizeof(float) * (size_t)g.splits * Z * N * M : 0;
@@ -305,16 +305,29 @@ GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max
     return g;
 }
 
+// Where the query projection's GEMM writes its heads (OUT_QROPE).
+struct QRopeOut {
+    __nv_bfloat16* q_nope;
+    __nv_bfloat16* q_pe;
+    const int32_t* positions;
+    int H, d_h, d_r;
+    const uint64_t* freq;  // rope::MAX_PAIRS fixed-point frequencies
+};
+
 // Launch the persistent GEMM.  ta2 serves the M tiles from m_split on (pass
-// ta and m_split = m_tiles when there is one A map).
+// ta and m_split = m_tiles when there is one A map).  With qo (a plan
+// without K splits) the epilogue writes the query heads instead of `out`.
 mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_split, const CUtensorMap& tx,
                          int M, int N, int K, int Z, int a_mn, int x_batched, const GemmPlan& g,
                          __nv_bfloat16* out, int64_t ldo, int64_t out_z, float* ws_part, int* ws_count,
-                         cudaStream_t st) {
+                         cudaStream_t st, const QRopeOut* qo = nullptr) {
     if (g.items < 1 || M % 8 != 0) return MLA_ERR_UNSUPPORTED;
     if (g.mode != mla::gemm::OUT_BF16 && (!ws_part || !aligned16(ws_part))) return MLA_ERR_INVALID_ARG;
     if (g.mode == mla::gemm::OUT_REDUCE && !ws_count) return MLA_ERR_INVALID_ARG;
-    mla::gemm::Params p;
+    if (qo && (g.mode != mla::gemm::OUT_BF16 || qo->d_h % 8 != 0 || qo->d_r % 8 != 0 ||
+               (int64_t)qo->H * (qo->d_h + qo->d_r) != M))
+        return MLA_ERR_UNSUPPORTED;
+    mla::gemm::Params p{};
     p.M = M;
     p.N = N;
     p.K = K;
@@ -338,6 +351,16 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
     p.out_z = out_z;
     p.ws_part = ws_part;
     p.ws_count = ws_count;
+    if (qo) {
+        p.mode = mla::gemm::OUT_QROPE;
+        p.q_nope = qo->q_nope;
+        p.q_pe = qo->q_pe;
+        p.positions = qo->positions;
+        p.q_heads = qo->H;
+        p.d_h = qo->d_h;
+        p.d_r = qo->d_r;
+        for (int k = 0; k < mla::rope::MAX_PAIRS; ++k) p.freq[k] = qo->freq[k];
+    }
     (void)Z;
     const mla_status_t s = launch_pdl(g.MT == 2 ? mla::gemm::wgemm_kernel<2> : mla::gemm::wgemm_kernel<1>,
                                       dim3((unsigned)g.grid), dim3(mla::gemm::THREADS), g.smem, st, ta, ta2,
@@ -769,13 +792,25 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
     return launch_status();
 }
 
+// The query projection's GEMM writes q_nope / q_pe itself, rotating q^R in
+// its epilogue, when its output tiles alone give at least half of the SMs
+// work; with fewer (few heads, a long K) it splits K into fp32 partials that
+// the finishing kernel adds up.  `fused` says which; the workspace is that
+// of the plan returned (none for the direct one).
+GemmPlan project_q_plan(int M, int N, int d, int sms, bool& fused) {
+    const GemmPlan direct = gemm_plan(M, N, d, 1, sms, kNoSplit);
+    fused = direct.items >= (sms + 1) / 2;
+    return fused ? direct : gemm_plan(M, N, d, 1, sms, kSplitParts);
+}
+
 size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype) {
     if (dtype != MLA_BF16 || N < 1 || H < 1 || d_h < 1 || d_r < 1 || d < 64) return 0;
     const int64_t M = (int64_t)H * (d_h + d_r);
     if (M % 128 != 0 || M > (1 << 30)) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    return plain_gemm_ws_bytes(gemm_plan((int)M, N, d, 1, di.sms, kSplitParts));
+    bool fused = false;
+    return plain_gemm_ws_bytes(project_q_plan((int)M, N, d, di.sms, fused));
 }
 
 mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
@@ -820,9 +855,21 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
         return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    const GemmPlan g = gemm_plan((int)M, N, d, 1, di.sms, kSplitParts);
-    if (!workspace || !aligned16(workspace) || workspace_bytes < plain_gemm_ws_bytes(g))
+    bool fused = false;
+    const GemmPlan g = project_q_plan((int)M, N, d, di.sms, fused);
+    const size_t need = plain_gemm_ws_bytes(g);
+    if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
         return MLA_ERR_INVALID_ARG;
+    if (fused) {
+        // W^Q h on the tensor cores, the epilogue splitting each row per
+        // head and rotating q^R before the one rounding: one launch
+        CUtensorMap ta, tx;
+        if (!weight_map(&ta, w_q, (int)M, d) || !rows_map(&tx, h, N, d, d, g.BN)) return MLA_ERR_CUDA;
+        const QRopeOut qo{static_cast<__nv_bfloat16*>(q_nope), static_cast<__nv_bfloat16*>(q_pe), positions,
+                          H, d_h, d_r, p.freq};
+        return launch_gemm(ta, ta, g.m_tiles, tx, (int)M, N, d, 1, 0, 0, g, nullptr, 0, 0, nullptr, nullptr, st,
+                           &qo);
+    }
     // W^Q h on the tensor cores, each K split's fp32 partial into the
     // workspace; then the finishing kernel adds the splits, splits each row
     // per head, rotates q^R and rounds once

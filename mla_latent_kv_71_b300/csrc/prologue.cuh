@@ -12,29 +12,23 @@
 // k^R shared by all heads; [llms] "Low-Rank Key-Value Joint Compression" and
 // "The Positional Problem and Decoupled RoPE".)
 //
-// RoPE rotates pair (x_2k, x_2k+1) of a d_r-vector by pos * base^(-2k/d_r)
-// (the pages fix only that the angle grows with the position; pairing and
-// frequencies are the common reading).  The angle is kept in turns: the host
-// passes each frequency f_k = base^(-2k/d_r) / 2pi as a 64-bit fixed-point
-// fraction F_k = round(f_k 2^64), and pos * F_k taken modulo 2^64 is the
-// fraction of a turn pos * f_k mod 1, exact up to pos times the rounding of
-// F_k (below 2^-33 of a turn for any int32 position).  Its top 24 bits,
-// rounded, give the angle to 2^-25 of a turn (2e-7 rad), and sin / cos come
-// from fp32 sincospif, whose argument needs no further reduction.  So
-// positions in the hundreds of thousands keep their phase without fp64
-// arithmetic (slow on this GPU).
+// RoPE: pair (x_2k, x_2k+1) rotated by pos * base^(-2k/d_r), the angle
+// taken in fixed-point turns without fp64 (rope.cuh).
 //
 // In bf16 mode the products W^DKV h, W^KR h and W^Q h run on the tensor-core
-// GEMM (gemm_bf16.cuh), which leaves each K split's fp32 partial in the
-// workspace; the finishing kernels here add the splits, rotate, round once
-// and scatter.  In fp32 mode the kernels here compute every row on CUDA
-// cores.
+// GEMM (gemm_bf16.cuh).  For the cache write, and for a query projection with
+// too few output tiles to fill the GPU, it leaves each K split's fp32 partial
+// in the workspace, and the finishing kernels here add the splits, rotate,
+// round once and scatter; a query projection whose tiles fill the GPU is
+// written by the GEMM's own epilogue (OUT_QROPE).  In fp32 mode the kernels
+// here compute every row on CUDA cores.
 #pragma once
 
 #include <cstdint>
 #include <cuda_bf16.h>
 
 #include "pdl.cuh"
+#include "rope.cuh"
 #include "status.cuh"
 
 namespace mla {
@@ -43,23 +37,24 @@ namespace pro {
 constexpr int THREADS = 256;  // 8 warps
 constexpr int TOK = 8;        // tokens per block (fp32 kernels)
 constexpr int ROWS = 8;       // weight rows (outputs) per block (fp32 kernels)
-constexpr int MAX_PAIRS = 64; // d_r <= 128
+constexpr int MAX_PAIRS = rope::MAX_PAIRS;  // d_r <= 128
 constexpr int Q_HEADS = 4;    // heads per block of the bf16 query finish
 
 // sum over the K splits, in split order, of the fp32 pair at src in each
-// split's partials (split_stride floats apart).  The loads of eight splits
-// are issued together: a split count in the tens would otherwise make this
-// a chain of dependent L2 round trips.
+// split's partials (split_stride floats apart).  The loads of up to
+// SUM_BATCH splits are issued together: a split count in the tens would
+// otherwise make this a chain of dependent L2 round trips.
+constexpr int SUM_BATCH = 16;
 __device__ __forceinline__ float2 sum_splits(const float* src, int64_t split_stride, int splits) {
     float a = 0.f, b = 0.f;
-    for (int s0 = 0; s0 < splits; s0 += 8) {
-        float2 v[8];
+    for (int s0 = 0; s0 < splits; s0 += SUM_BATCH) {
+        float2 v[SUM_BATCH];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < SUM_BATCH; ++k)
             v[k] = s0 + k < splits ? __ldcg(reinterpret_cast<const float2*>(src + (s0 + k) * split_stride))
                                    : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < SUM_BATCH; ++k) {
             a += v[k].x;
             b += v[k].y;
         }
@@ -67,18 +62,8 @@ __device__ __forceinline__ float2 sum_splits(const float* src, int64_t split_str
     return make_float2(a, b);
 }
 
-// sin and cos of the angle pos * f, f given as the 0.64 fixed-point
-// fraction of a turn described above.
-__device__ __forceinline__ void rope_sincos(int64_t pos, uint64_t f, float& sn, float& cs) {
-    const uint64_t t = static_cast<uint64_t>(pos) * f;  // fraction of a turn, mod 1
-    const uint32_t top = static_cast<uint32_t>((t + (1ull << 39)) >> 40);  // 24 bits, rounded
-    sincospif(2.0f * (static_cast<float>(top) * 0x1p-24f), &sn, &cs);
-}
-
-__device__ __forceinline__ void rotate(float a, float b, float sn, float cs, float& ya, float& yb) {
-    ya = fmaf(a, cs, -b * sn);
-    yb = fmaf(a, sn, b * cs);
-}
+using rope::rope_sincos;
+using rope::rotate;
 
 // 16 bytes of T widened to fp32 (bf16 -> fp32 is exact: the bits move up).
 __device__ __forceinline__ void widen(const uint4& v, float (&f)[4]) {

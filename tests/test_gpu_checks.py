@@ -92,6 +92,23 @@ torch.cuda.synchronize()
 ref, _ = oracle.out_proj(o.cpu(), w_uv.cpu(), w_o.cpu())
 check(out, ref, "out_proj")
 
+# the query projection written by the GEMM's epilogue (heads split, q^R rotated)
+N, H, d_h, d_r, d_q = 40, 128, 128, 64, 1536
+ch = torch.randn((N, d_q), generator=g, device=dev).to(torch.bfloat16)
+w_q = workloads.weight((H * (d_h + d_r), d_q), d_q, g, dev, torch.bfloat16)
+pos = torch.randint(0, 100001, (N,), generator=g, device=dev, dtype=torch.int32)
+qn = torch.full((N, H, d_h), float("nan"), device=dev).to(torch.bfloat16)
+qp = torch.full((N, H, d_r), float("nan"), device=dev).to(torch.bfloat16)
+mla.project_q(ch, w_q, pos, H, d_h, d_r, qn, qp)
+torch.cuda.synchronize()
+_, qn_ref, qp_ref = oracle.project(ch.cpu().reshape(N, 1, d_q), torch.zeros((2, d_q), dtype=torch.bfloat16),
+                                   torch.zeros((d_r, d_q), dtype=torch.bfloat16), w_q.cpu(), H, d_h, qpos=0)
+for n, ps in enumerate(pos.tolist()):
+    for i in range(H):
+        qp_ref[n, i] = oracle.rope(qp_ref[n, i], ps)
+check(qn, qn_ref, "project_q content")
+check(qp, qp_ref, "project_q rotated")
+
 # the prefill attention (causal, a ragged last block)
 case = workloads.prefill_case(1, 300, 4, d=1024, seed=94, device=dev)
 k, v = mla.prefill_expand(case.kv, case.w_uk, case.w_uv)

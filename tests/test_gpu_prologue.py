@@ -204,20 +204,31 @@ def test_bf16_cache_append_model_widths(N):
     assert _untouched(pool_d.cpu(), table, seqs, positions)
 
 
-def test_bf16_project_q_compressed_query_widths():
-    """The compressed query c^Q (1536 wide) to 128 heads x [128 ; 64], at
-    positions up to 10^5."""
-    N, d, H, d_h, d_r = 19, 1536, 128, 128, 64
-    g = torch.Generator().manual_seed(50)
+@pytest.mark.parametrize("N,d,H,d_h,d_r", [
+    (19, 1536, 128, 128, 64),   # c^Q -> 128 x [128 ; 64]: the GEMM writes the heads (one N tile)
+    (64, 1536, 128, 128, 64),   # the decode batch of the headline workload
+    (300, 1024, 32, 128, 64),   # two N tiles, the second ragged
+    (37, 1024, 128, 64, 32),    # heads of 96 rows straddle the GEMM's 128-row tiles
+    (23, 1536, 8, 128, 64),     # few heads: K split into partials, then the finishing kernel
+])
+def test_bf16_project_q_widths(N, d, H, d_h, d_r):
+    """The query projection at model widths, positions up to 10^5, against
+    the oracle: content part within the bf16 bar, RoPE part within it
+    relative to the length of each rotated pair."""
+    g = torch.Generator().manual_seed(50 + N)
     h = torch.randn((N, d), generator=g).to(torch.bfloat16)
     w_q = workloads.weight((H * (d_h + d_r), d), d, g, "cpu", torch.bfloat16)
     positions = torch.randint(0, 100001, (N,), generator=g, dtype=torch.int32)
-    qn, qp = mla.project_q(h.cuda(), w_q.cuda(), positions.cuda(), H, d_h, d_r)
+    qn = torch.full((N, H, d_h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    qp = torch.full((N, H, d_r), float("nan"), dtype=torch.bfloat16, device="cuda")
+    mla.project_q(h.cuda(), w_q.cuda(), positions.cuda(), H, d_h, d_r, qn, qp)
     torch.cuda.synchronize()
+    assert mla.get_device_status()[0] == 0
     qn_ref, qp_ref = _oracle_query(h, w_q, positions, H, d_h, d_r)
     ok, err = _bf16_close(qn, qn_ref)
     assert ok, f"max |q^C - q^C*| = {err:.3e}"
     got = qp.float().cpu().double().numpy()
+    assert np.isfinite(got).all()
     pair = np.sqrt(qp_ref[..., 0::2] ** 2 + qp_ref[..., 1::2] ** 2).repeat(2, axis=-1)
     excess = (np.abs(got - qp_ref) - (2 * BF16_REL * pair + BF16_ABS)).max()
     assert excess <= 0, f"max |q^R - q^R*| = {np.abs(got - qp_ref).max():.3e}"
