@@ -188,19 +188,35 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
         }
         epi_sync();
         const int ncols = min(EPI_COLS, n_valid - c0);
+        // Thread t always takes the same rows of the tile (a 16-byte piece
+        // of 4 fp32 or 8 bf16 rows) and every 4th / 8th token column.  Each
+        // batch of pieces is read from the staging rows first and then
+        // stored, so that the stores issue back to back (one load, one
+        // store per step ran ~3x slower).
         if (fp32) {
-            float* base = p.ws_part + (((int64_t)w.split * Z + w.z) * p.N + n0 + c0) * p.M + m0;
-            for (int idx = t; idx < ncols * 32; idx += BM) {
-                const int j = idx >> 5, m = (idx & 31) * 4;
-                if (m < mv)
-                    *reinterpret_cast<float4*>(base + (int64_t)j * p.M + m) =
-                        *reinterpret_cast<const float4*>(stg_f + j * BM + m);
+            constexpr int PIECES = EPI_COLS * 32 / BM;  // float4 pieces per thread and round
+            const int m = (t & 31) * 4;
+            float* base = p.ws_part + (((int64_t)w.split * Z + w.z) * p.N + n0 + c0) * p.M + m0 + m;
+#pragma unroll
+            for (int h = 0; h < PIECES; h += 8) {
+                float4 v[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int j = (t >> 5) + (h + k) * (BM / 32);
+                    v[k] = j < ncols ? *reinterpret_cast<const float4*>(stg_f + j * BM + m)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+                if (m < mv) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int j = (t >> 5) + (h + k) * (BM / 32);
+                        if (j < ncols) *reinterpret_cast<float4*>(base + (int64_t)j * p.M) = v[k];
+                    }
+                }
             }
         } else if (qrope) {
-            // 8 rows (one 16-byte store) of one token per step.  Thread t
-            // always takes rows 8 (t % 16) .. +7 of the tile (BM is a
-            // multiple of 16), so its head, part and frequencies are fixed
-            // for the tile and only the token changes.
+            // The head, part and frequencies of the thread's 8 rows are fixed
+            // for the tile; only the token changes.
             const int m = (t & 15) * 8;
             const int qw = p.d_h + p.d_r, row = m0 + m;
             const int i = row / qw, f = row - i * qw;
@@ -210,38 +226,49 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
             for (int k = 0; k < 4; ++k) fr[k] = rot ? freq[(f - p.d_h) / 2 + k] : 0;
             __nv_bfloat16* dst0 = rot ? p.q_pe + (int64_t)i * p.d_r + (f - p.d_h) : p.q_nope + (int64_t)i * p.d_h + f;
             const int64_t tok_stride = (int64_t)p.q_heads * (rot ? p.d_r : p.d_h);
+            // (one piece at a time: unrolled, the rotations' code made the
+            // whole kernel slower)
             if (m < mv)
                 for (int j = t >> 4; j < ncols; j += BM / 16) {
-                    const int n = n0 + c0 + j;
                     const float4 lo = *reinterpret_cast<const float4*>(stg_f + j * BM + m);
                     const float4 hi = *reinterpret_cast<const float4*>(stg_f + j * BM + m + 4);
                     float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                     if (rot) {
-                        const int64_t pos = pos_s[j + c0];
+                        const int64_t pos = pos_s[c0 + j];
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
+                        for (int q = 0; q < 4; ++q) {
                             float sn, cs;
-                            rope::rope_sincos(pos, fr[k], sn, cs);
-                            rope::rotate(v[2 * k], v[2 * k + 1], sn, cs, v[2 * k], v[2 * k + 1]);
+                            rope::rope_sincos(pos, fr[q], sn, cs);
+                            rope::rotate(v[2 * q], v[2 * q + 1], sn, cs, v[2 * q], v[2 * q + 1]);
                         }
                     }
-                    *reinterpret_cast<uint4*>(dst0 + n * tok_stride) =
+                    *reinterpret_cast<uint4*>(dst0 + (int64_t)(n0 + c0 + j) * tok_stride) =
                         make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
                                    pack2_bf16(v[6], v[7]));
                 }
         } else {
-            __nv_bfloat16* base = p.out + (int64_t)(n0 + c0) * p.ldo + (int64_t)w.z * p.out_z + m0;
-            for (int idx = t; idx < ncols * 16; idx += BM) {
-                const int j = idx >> 4, m = (idx & 15) * 8;
-                if (m >= mv) continue;
-                const uint4 v = *reinterpret_cast<const uint4*>(stg_h + j * BM + m);
-                __nv_bfloat16* dst = base + (int64_t)j * p.ldo + m;
-                if (p.vec_out) {
-                    *reinterpret_cast<uint4*>(dst) = v;
-                } else {
-                    const uint16_t* e = reinterpret_cast<const uint16_t*>(&v);
+            constexpr int PIECES = EPI_COLS * 16 / BM;  // 8
+            const int m = (t & 15) * 8;
+            __nv_bfloat16* base = p.out + (int64_t)(n0 + c0) * p.ldo + (int64_t)w.z * p.out_z + m0 + m;
+            uint4 v[PIECES];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) reinterpret_cast<uint16_t*>(dst)[k] = e[k];
+            for (int k = 0; k < PIECES; ++k) {
+                const int j = (t >> 4) + k * (BM / 16);
+                v[k] = j < ncols ? *reinterpret_cast<const uint4*>(stg_h + j * BM + m) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            if (m < mv) {
+#pragma unroll
+                for (int k = 0; k < PIECES; ++k) {
+                    const int j = (t >> 4) + k * (BM / 16);
+                    if (j >= ncols) continue;
+                    __nv_bfloat16* dst = base + (int64_t)j * p.ldo;
+                    if (p.vec_out) {
+                        *reinterpret_cast<uint4*>(dst) = v[k];
+                    } else {
+                        const uint16_t* e = reinterpret_cast<const uint16_t*>(&v[k]);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) reinterpret_cast<uint16_t*>(dst)[q] = e[q];
+                    }
                 }
             }
         }
