@@ -42,7 +42,10 @@
  *   - The projection GEMMs and the prologue's second kernels are launched
  *     with programmatic stream serialization: they may start their set-up
  *     while the kernel before them on the stream finishes, and wait for it
- *     before touching global memory.  They also let the next kernel launch
+ *     before touching memory it writes or reads (the cache write's second
+ *     kernel looks up its pool rows in the call's inputs first: that kernel
+ *     is the call's own GEMM, which writes only its partials).  They also
+ *     let the next kernel launch
  *     early; a kernel of the caller's launched that way must wait
  *     (griddepcontrol.wait) before reading what they write.
  *   - The prefill calls (mla_prefill_*) and the merged-query calls also

@@ -299,6 +299,10 @@ GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max
     const size_t stage = (size_t)g.MT * mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
     const size_t fixed = mla::gemm::FIXED_SMEM;
     g.stages = (int)std::min<size_t>(mla::gemm::MAX_STAGES, (mla::gemm::SMEM_CAP - fixed) / stage);
+    // no more stages than the busiest CTA has K chunks: the rest of the
+    // shared memory is then free for a dependent kernel's blocks
+    const int64_t busiest = (items + g.grid - 1) / std::max(1, g.grid) * g.chunks;
+    g.stages = (int)std::max<int64_t>(2, std::min<int64_t>(g.stages, busiest));
     g.smem = fixed + (size_t)g.stages * stage;
     g.ws_part_bytes = g.mode != mla::gemm::OUT_BF16 ? sizeof(float) * (size_t)g.splits * Z * N * M : 0;
     g.ws_count_bytes = g.mode == mla::gemm::OUT_REDUCE ? sizeof(int) * (size_t)tiles : 0;

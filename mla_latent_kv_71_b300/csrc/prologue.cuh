@@ -208,21 +208,22 @@ __global__ void __launch_bounds__(THREADS) kv_rows_fp32_kernel(const KvParams p)
 // it, so that the block writes the whole pool row in one pass.
 __global__ void kv_finish_bf16_kernel(const KvParams p) {
     __shared__ __nv_bfloat16* row;
-    grid_dep_wait();  // the GEMM's partials (launched as its dependent, pdl.cuh)
-    if (threadIdx.x == 0) row = device_status_raised() ? nullptr : kv_row<__nv_bfloat16>(p, blockIdx.x);
-    __syncthreads();
-    if (row == nullptr) return;
+    const int n = blockIdx.x;
     const int E = p.d_c + p.d_r;
     const int e = 2 * (int)threadIdx.x;
-    if (e >= E) return;
-    const int n = blockIdx.x;
+    // The pool row and the rotation depend only on the call's inputs, which
+    // are complete before the GEMM ahead lets this kernel launch (pdl.cuh):
+    // look them up while the GEMM finishes, then wait for its partials.
+    if (threadIdx.x == 0) row = kv_row<__nv_bfloat16>(p, n);
+    float sn = 0.f, cs = 1.f;
+    if (e >= p.d_c && e < E) rope_sincos(p.positions[n], p.freq[(e - p.d_c) / 2], sn, cs);
+    grid_dep_wait();
+    if (threadIdx.x == 0 && device_status_raised()) row = nullptr;
+    __syncthreads();
+    if (row == nullptr || e >= E) return;
     const float2 ab = sum_splits(p.parts + (int64_t)n * E + e, (int64_t)p.N * E, p.splits);
     float a = ab.x, b = ab.y;
-    if (e >= p.d_c) {
-        float sn, cs;
-        rope_sincos(p.positions[n], p.freq[(e - p.d_c) / 2], sn, cs);
-        rotate(a, b, sn, cs, a, b);
-    }
+    if (e >= p.d_c) rotate(a, b, sn, cs, a, b);
     *reinterpret_cast<__nv_bfloat162*>(row + e) = __floats2bfloat162_rn(a, b);
 }
 
