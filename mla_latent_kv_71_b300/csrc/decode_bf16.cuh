@@ -1071,11 +1071,15 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                                 pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv_l, __uint_as_float(r[8 * v + 5]) * inv_l),
                                 pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv_l, __uint_as_float(r[8 * v + 7]) * inv_l));
                         __syncwarp();
+                        // the pieces are read first, then stored back to back
+                        // (a read before each store ran the stores ~3x slower)
+                        uint4 piece[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) piece[k] = *stg(8 * k + (lane >> 2), lane & 3);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {  // 8 rows x 64 bytes per store
                             const int row = 8 * k + (lane >> 2);
-                            if (head0 + row < p.H)
-                                *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 3);
+                            if (head0 + row < p.H) *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = piece[k];
                         }
                         __syncwarp();
                     }
@@ -1098,11 +1102,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_consta
                                                        __float_as_uint(__uint_as_float(r[4 * v + 2]) * inv_l),
                                                        __float_as_uint(__uint_as_float(r[4 * v + 3]) * inv_l));
                         __syncwarp();
+                        uint4 piece[8];
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) piece[k] = *stg(4 * k + (lane >> 3), lane & 7);
 #pragma unroll
                         for (int k = 0; k < 8; ++k) {  // 4 rows x 128 bytes per store
                             const int row = 4 * k + (lane >> 3);
-                            if (row < live_rows)
-                                *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = *stg(row, lane & 7);
+                            if (row < live_rows) *reinterpret_cast<uint4*>(dst + (int64_t)row * DC + cc) = piece[k];
                         }
                         __syncwarp();
                     }
