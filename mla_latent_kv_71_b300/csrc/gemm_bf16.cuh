@@ -62,6 +62,7 @@ constexpr int STG_BYTES = EPI_COLS * BM * 4;    // 32 KB (fp32 rows of 128)
 constexpr int CTL_BYTES = 256;                  // barriers, TMEM address, reducer flag
 constexpr int FREQ_BYTES = rope::MAX_PAIRS * 8; // OUT_QROPE: the RoPE frequencies
 constexpr int POS_BYTES = 256 * 4;              // OUT_QROPE: positions of an N tile's tokens
+constexpr int ROPE_TABLE_MAX = 16 * 1024;       // OUT_QROPE: largest sin/cos table kept in shared memory
 // shared memory besides the ring: 1 KB alignment slack, staging, control,
 // frequencies, positions
 constexpr int FIXED_SMEM = 1024 + STG_BYTES + CTL_BYTES + FREQ_BYTES + POS_BYTES;
@@ -100,6 +101,8 @@ struct Params {
     __nv_bfloat16* q_pe;
     const int32_t* positions;
     int q_heads, d_h, d_r;
+    int rope_table;       // sin, cos of every (token, pair) of the N tile precomputed in shared memory
+                          // (BN x d_r/2 float2 after the fixed area; the planner adds its bytes)
     uint64_t freq[rope::MAX_PAIRS];
 };
 
@@ -152,8 +155,8 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // warp on that barrier) as soon as the last round's columns are in
 // registers.
 __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int mt, int Z, uint32_t tacc,
-                                           uint8_t* stg, const uint64_t* freq, const int32_t* pos_s, int t,
-                                           bool fp32, uint32_t release) {
+                                           uint8_t* stg, const uint64_t* freq, const int32_t* pos_s,
+                                           const float2* tab, int t, bool fp32, uint32_t release) {
     const int m0 = mt * BM, n0 = w.nt * p.BN;
     const int n_valid = min(p.BN, p.N - n0);
     const int mv = min(BM, p.M - m0);
@@ -226,9 +229,42 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
             for (int k = 0; k < 4; ++k) fr[k] = rot ? freq[(f - p.d_h) / 2 + k] : 0;
             __nv_bfloat16* dst0 = rot ? p.q_pe + (int64_t)i * p.d_r + (f - p.d_h) : p.q_nope + (int64_t)i * p.d_h + f;
             const int64_t tok_stride = (int64_t)p.q_heads * (rot ? p.d_r : p.d_h);
-            // (one piece at a time: unrolled, the rotations' code made the
-            // whole kernel slower)
-            if (m < mv)
+            if (p.rope_table) {
+                // sin and cos from the N tile's table: the pieces are read,
+                // rotated and packed first, then stored back to back
+                constexpr int PIECES = EPI_COLS * 16 / BM;  // 8
+                const int pairs = p.d_r / 2, k0 = rot ? (f - p.d_h) / 2 : 0;
+                if (m < mv) {
+                    uint4 packed[PIECES];
+#pragma unroll
+                    for (int k = 0; k < PIECES; ++k) {
+                        const int j = (t >> 4) + k * (BM / 16);
+                        if (j >= ncols) continue;
+                        const float4 lo = *reinterpret_cast<const float4*>(stg_f + j * BM + m);
+                        const float4 hi = *reinterpret_cast<const float4*>(stg_f + j * BM + m + 4);
+                        float v[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                        if (rot) {
+                            // (sn, cs) of pairs k0 .. k0+3: 32 bytes, 16-byte aligned (k0 % 4 == 0)
+                            const float4* sc = reinterpret_cast<const float4*>(tab + (c0 + j) * pairs + k0);
+                            const float4 a = sc[0], b = sc[1];
+                            rope::rotate(v[0], v[1], a.x, a.y, v[0], v[1]);
+                            rope::rotate(v[2], v[3], a.z, a.w, v[2], v[3]);
+                            rope::rotate(v[4], v[5], b.x, b.y, v[4], v[5]);
+                            rope::rotate(v[6], v[7], b.z, b.w, v[6], v[7]);
+                        }
+                        packed[k] = make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]),
+                                               pack2_bf16(v[4], v[5]), pack2_bf16(v[6], v[7]));
+                    }
+#pragma unroll
+                    for (int k = 0; k < PIECES; ++k) {
+                        const int j = (t >> 4) + k * (BM / 16);
+                        if (j < ncols)
+                            *reinterpret_cast<uint4*>(dst0 + (int64_t)(n0 + c0 + j) * tok_stride) = packed[k];
+                    }
+                }
+            } else if (m < mv) {
+                // no table (large N tiles): one piece at a time, its angles
+                // computed here (unrolled, that code slowed the whole kernel)
                 for (int j = t >> 4; j < ncols; j += BM / 16) {
                     const float4 lo = *reinterpret_cast<const float4*>(stg_f + j * BM + m);
                     const float4 hi = *reinterpret_cast<const float4*>(stg_f + j * BM + m + 4);
@@ -246,6 +282,7 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
                         make_uint4(pack2_bf16(v[0], v[1]), pack2_bf16(v[2], v[3]), pack2_bf16(v[4], v[5]),
                                    pack2_bf16(v[6], v[7]));
                 }
+            }
         } else {
             constexpr int PIECES = EPI_COLS * 16 / BM;  // 8
             const int m = (t & 15) * 8;
@@ -352,6 +389,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     int* flag = reinterpret_cast<int*>(tmem_slot + 1);  // [0] this tile's reducer
     uint64_t* freq_s = reinterpret_cast<uint64_t*>(stg + STG_BYTES + CTL_BYTES);
     int32_t* pos_s = reinterpret_cast<int32_t*>(stg + STG_BYTES + CTL_BYTES + FREQ_BYTES);
+    float2* tab_s = reinterpret_cast<float2*>(stg + STG_BYTES + CTL_BYTES + FREQ_BYTES + POS_BYTES);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int i0 = (int)((int64_t)p.items * blockIdx.x / gridDim.x);
@@ -521,6 +559,15 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                 pos_nt = w.nt;
                 for (int j = t; j < p.BN; j += BM)
                     pos_s[j] = w.nt * p.BN + j < p.N ? __ldg(p.positions + w.nt * p.BN + j) : 0;
+                if (p.rope_table) {
+                    const int pairs = p.d_r / 2;
+                    for (int e = t; e < p.BN * pairs; e += BM) {
+                        const int j = e / pairs, n = w.nt * p.BN + j;
+                        float sn = 0.f, cs = 1.f;
+                        if (n < p.N) rope::rope_sincos(__ldg(p.positions + n), freq_s[e - j * pairs], sn, cs);
+                        tab_s[e] = make_float2(sn, cs);
+                    }
+                }
             }
             bool good = ok && __all_sync(0xffffffffu, mbar_wait(accf0 + 8 * b, use & 1, 0x104));
             good = epi_sync_and(good);
@@ -532,7 +579,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                 // the last tile's final TMEM read hands the buffer back
                 if (good)
                     store_tile(p, w, mt, Z, tmem + b * acc_cols + (uint32_t)(j * p.BN) + ((uint32_t)(q * 32) << 16),
-                               stg, freq_s, pos_s, t, p.mode == OUT_REDUCE || p.mode == OUT_PARTS,
+                               stg, freq_s, pos_s, tab_s, t, p.mode == OUT_REDUCE || p.mode == OUT_PARTS,
                                j == MT - 1 ? acce0 + 8 * b : 0u);
                 if (p.mode == OUT_REDUCE) {
                     // Every CTA of a split tile arrives on its counter -- also

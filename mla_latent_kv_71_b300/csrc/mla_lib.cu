@@ -249,7 +249,7 @@ enum SplitMode : int { kNoSplit = 0, kSplitReduce = 1, kSplitParts = 2 };
 // considered only for few output tiles and a workspace below 256 MB; of two
 // plans within 2 % of each other the one with fewer TMA rows per CTA wins.
 GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max_splits = 64,
-                   bool allow_pairs = true) {
+                   bool allow_pairs = true, size_t extra_smem = 0) {
     const double kRow = 3.1, kHbm = 3150.0, kStore = 20.0, kL2 = 64.0;
     GemmPlan g;
     g.BN = N >= 256 ? 256 : ((N + 15) / 16) * 16;
@@ -297,7 +297,7 @@ GemmPlan gemm_plan(int M, int N, int K, int Z, int sms, SplitMode split, int max
     g.items = items > 0x7FFFFFFF ? 0 : (int)items;  // 0: too large (refused by the caller)
     g.grid = (int)std::min<int64_t>(items, sms);
     const size_t stage = (size_t)g.MT * mla::gemm::A_BYTES + (size_t)g.BN * mla::gemm::BK * 2;
-    const size_t fixed = mla::gemm::FIXED_SMEM;
+    const size_t fixed = mla::gemm::FIXED_SMEM + extra_smem;  // extra: the query's rotation table
     g.stages = (int)std::min<size_t>(mla::gemm::MAX_STAGES, (mla::gemm::SMEM_CAP - fixed) / stage);
     // no more stages than the busiest CTA has K chunks: the rest of the
     // shared memory is then free for a dependent kernel's blocks
@@ -316,6 +316,7 @@ struct QRopeOut {
     const int32_t* positions;
     int H, d_h, d_r;
     const uint64_t* freq;  // rope::MAX_PAIRS fixed-point frequencies
+    int table;             // the plan reserved the N tile's sin/cos table
 };
 
 // Launch the persistent GEMM.  ta2 serves the M tiles from m_split on (pass
@@ -363,6 +364,7 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
         p.q_heads = qo->H;
         p.d_h = qo->d_h;
         p.d_r = qo->d_r;
+        p.rope_table = qo->table;
         for (int k = 0; k < mla::rope::MAX_PAIRS; ++k) p.freq[k] = qo->freq[k];
     }
     (void)Z;
@@ -800,11 +802,23 @@ mla_status_t mla_cache_append(const void* h, const void* w_dkv, const void* w_kr
 // its epilogue, when its output tiles alone give at least half of the SMs
 // work; with fewer (few heads, a long K) it splits K into fp32 partials that
 // the finishing kernel adds up.  `fused` says which; the workspace is that
-// of the plan returned (none for the direct one).
-GemmPlan project_q_plan(int M, int N, int d, int sms, bool& fused) {
-    const GemmPlan direct = gemm_plan(M, N, d, 1, sms, kNoSplit);
+// of the plan returned (none for the direct one).  A direct plan whose N
+// tile's sin / cos table (BN x d_r/2 pairs) fits ROPE_TABLE_MAX keeps it in
+// shared memory (`table`), planned with those bytes taken from the ring.
+GemmPlan project_q_plan(int M, int N, int d, int d_r, int sms, bool& fused, bool& table) {
+    GemmPlan direct = gemm_plan(M, N, d, 1, sms, kNoSplit);
     fused = direct.items >= (sms + 1) / 2;
-    return fused ? direct : gemm_plan(M, N, d, 1, sms, kSplitParts);
+    table = false;
+    if (!fused) return gemm_plan(M, N, d, 1, sms, kSplitParts);
+    const size_t tab = (size_t)direct.BN * (d_r / 2) * sizeof(float2);
+    if (tab <= (size_t)mla::gemm::ROPE_TABLE_MAX) {
+        const GemmPlan with = gemm_plan(M, N, d, 1, sms, kNoSplit, 64, true, tab);
+        if (with.BN == direct.BN) {
+            table = true;
+            return with;
+        }
+    }
+    return direct;
 }
 
 size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_dtype_t dtype) {
@@ -813,8 +827,8 @@ size_t mla_project_q_workspace_size(int N, int H, int d_h, int d_r, int d, mla_d
     if (M % 128 != 0 || M > (1 << 30)) return 0;
     DeviceInfo di;
     if (!device_info(di)) return 0;
-    bool fused = false;
-    return plain_gemm_ws_bytes(project_q_plan((int)M, N, d, di.sms, fused));
+    bool fused = false, table = false;
+    return plain_gemm_ws_bytes(project_q_plan((int)M, N, d, d_r, di.sms, fused, table));
 }
 
 mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positions, void* q_nope,
@@ -859,8 +873,8 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
         return MLA_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(di)) return MLA_ERR_CUDA;
-    bool fused = false;
-    const GemmPlan g = project_q_plan((int)M, N, d, di.sms, fused);
+    bool fused = false, table = false;
+    const GemmPlan g = project_q_plan((int)M, N, d, d_r, di.sms, fused, table);
     const size_t need = plain_gemm_ws_bytes(g);
     if (need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
         return MLA_ERR_INVALID_ARG;
@@ -870,7 +884,7 @@ mla_status_t mla_project_q(const void* h, const void* w_q, const int32_t* positi
         CUtensorMap ta, tx;
         if (!weight_map(&ta, w_q, (int)M, d) || !rows_map(&tx, h, N, d, d, g.BN)) return MLA_ERR_CUDA;
         const QRopeOut qo{static_cast<__nv_bfloat16*>(q_nope), static_cast<__nv_bfloat16*>(q_pe), positions,
-                          H, d_h, d_r, p.freq};
+                          H, d_h, d_r, p.freq, table ? 1 : 0};
         return launch_gemm(ta, ta, g.m_tiles, tx, (int)M, N, d, 1, 0, 0, g, nullptr, 0, 0, nullptr, nullptr, st,
                            &qo);
     }
