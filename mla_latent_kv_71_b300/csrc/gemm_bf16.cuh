@@ -154,6 +154,7 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 // `stg`.  When release != 0 the TMEM buffer is handed back (one arrival per
 // warp on that barrier) as soon as the last round's columns are in
 // registers.
+template <bool QR>
 __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int mt, int Z, uint32_t tacc,
                                            uint8_t* stg, const uint64_t* freq, const int32_t* pos_s,
                                            const float2* tab, int t, bool fp32, uint32_t release) {
@@ -162,7 +163,7 @@ __device__ __forceinline__ void store_tile(const Params& p, const Item& w, int m
     const int mv = min(BM, p.M - m0);
     float* stg_f = reinterpret_cast<float*>(stg);
     uint16_t* stg_h = reinterpret_cast<uint16_t*>(stg);
-    const bool qrope = p.mode == OUT_QROPE;
+    constexpr bool qrope = QR;  // p.mode == OUT_QROPE
     const bool stage32 = fp32 || qrope;
     for (int c0 = 0; c0 < n_valid; c0 += EPI_COLS) {
         uint32_t r[64];
@@ -370,8 +371,10 @@ __device__ __forceinline__ void reduce_tile(const Params& p, const Item& w, int 
 }
 
 // MT (M tiles per item, 1 or 2) is a template parameter: with it known at
-// compile time the product and copy issue loops unroll.
-template <int MT>
+// compile time the product and copy issue loops unroll.  QR (the query
+// output mode, OUT_QROPE) is one too, so that the other modes' kernels
+// carry none of its code.
+template <int MT, bool QR>
 __global__ void __launch_bounds__(THREADS, 1)
 wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a2,
              const __grid_constant__ CUtensorMap tm_x, const Params p) {
@@ -416,7 +419,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         flag[0] = 0;
         // the frequencies in shared memory: the epilogue's threads index
         // them by row, which the constant bank would serialise
-        if (p.mode == OUT_QROPE)
+        if (QR)
             for (int k = 0; k < rope::MAX_PAIRS; ++k) freq_s[k] = p.freq[k];
         fence_mbar_init_cluster();
     }
@@ -553,7 +556,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
         for (int item = i0; item < i1; ++item, ++acc) {
             const Item w = decode_item(p, item);
             const uint32_t b = acc & 1, use = acc >> 1;
-            if (p.mode == OUT_QROPE && w.nt != pos_nt) {
+            if (QR && w.nt != pos_nt) {
                 // the N tile's token positions, read while the products run
                 // (the previous item's stores, which read them, are done)
                 pos_nt = w.nt;
@@ -578,7 +581,7 @@ wgemm_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
                 const int mt = w.mt + j;
                 // the last tile's final TMEM read hands the buffer back
                 if (good)
-                    store_tile(p, w, mt, Z, tmem + b * acc_cols + (uint32_t)(j * p.BN) + ((uint32_t)(q * 32) << 16),
+                    store_tile<QR>(p, w, mt, Z, tmem + b * acc_cols + (uint32_t)(j * p.BN) + ((uint32_t)(q * 32) << 16),
                                stg, freq_s, pos_s, tab_s, t, p.mode == OUT_REDUCE || p.mode == OUT_PARTS,
                                j == MT - 1 ? acce0 + 8 * b : 0u);
                 if (p.mode == OUT_REDUCE) {

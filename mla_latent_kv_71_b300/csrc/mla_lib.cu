@@ -91,9 +91,13 @@ bool device_info(DeviceInfo& out) {
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::dec::SMEM_ALLOC) != cudaSuccess)
             return false;
-        if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(mla::gemm::wgemm_kernel<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::gemm::SMEM_CAP) != cudaSuccess ||
-            cudaFuncSetAttribute(mla::gemm::wgemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(mla::gemm::wgemm_kernel<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mla::gemm::SMEM_CAP) != cudaSuccess ||
+            cudaFuncSetAttribute(mla::gemm::wgemm_kernel<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)mla::gemm::SMEM_CAP) != cudaSuccess ||
+            cudaFuncSetAttribute(mla::gemm::wgemm_kernel<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)mla::gemm::SMEM_CAP) != cudaSuccess)
             return false;
         if (cudaFuncSetAttribute(mla::pre::prefill_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -368,7 +372,8 @@ mla_status_t launch_gemm(const CUtensorMap& ta, const CUtensorMap& ta2, int m_sp
         for (int k = 0; k < mla::rope::MAX_PAIRS; ++k) p.freq[k] = qo->freq[k];
     }
     (void)Z;
-    const mla_status_t s = launch_pdl(g.MT == 2 ? mla::gemm::wgemm_kernel<2> : mla::gemm::wgemm_kernel<1>,
+    const mla_status_t s = launch_pdl(qo ? (g.MT == 2 ? mla::gemm::wgemm_kernel<2, true> : mla::gemm::wgemm_kernel<1, true>)
+                                         : (g.MT == 2 ? mla::gemm::wgemm_kernel<2, false> : mla::gemm::wgemm_kernel<1, false>),
                                       dim3((unsigned)g.grid), dim3(mla::gemm::THREADS), g.smem, st, ta, ta2,
                                       tx, p);
     if (s != MLA_OK) return s;
